@@ -1,0 +1,179 @@
+"""Float64 CPU oracle for exact softmax attention and its split-KV form.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+(``attention_forward_05_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, IEEE double, single thread, no
+FMA contraction); this module compiles it with gcc and wraps it with ctypes.
+``forms.py`` holds the pages' other, slower formulations (2-pass, 1-pass tiled,
+KV-outer Algorithm 1, blocked-concatenation) written in numpy, used only as
+cross-checks of the plain definition; ``brute.py`` holds an mpmath brute force.
+
+Sources (web pages, cited by title and section):
+  [T1] "FlashAttention 简化版：Tiling + Online Softmax" (forceinjection.github.io)
+  [T2] "Flash Attention 代码填空 (Level 2-3)" (boots-coder.github.io, LLM-101-CN)
+  [T3] "CS349E 第 11 讲 01_online_softmax.py" (semidirectx.com)
+  [T4] "从零手写 FlashAttention（PyTorch实现 + 原理推导）" (mokono.cn)
+
+Definition followed: S = Q K^T * scale, P = row-softmax(S) with the row maximum
+subtracted, O = P V, LSE = m + ln(l) ([T1] §1.1, §2.1; [T2] Exercise 1;
+[T3] attn_row_3pass and demo 2).  Partial states (m, l, o) with o unnormalised
+and their merge follow [T3] demo 2.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library with gcc; returns its path.
+
+    ``-ffp-contract=off`` keeps gcc from fusing multiply-adds (its default on
+    aarch64), so the oracle rounds the same way on every host.
+    """
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.fao_attention_head.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long,
+                                               ctypes.c_long, ctypes.c_long, ctypes.c_double]
+            lib.fao_attention_head.restype = ctypes.c_int
+            lib.fao_attention.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                          ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double]
+            lib.fao_attention.restype = ctypes.c_int
+            lib.fao_partial_state.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                              ctypes.c_double, _dp, _dp, _dp]
+            lib.fao_partial_state.restype = ctypes.c_int
+            lib.fao_merge_states.argtypes = [ctypes.c_double, ctypes.c_double, _dp, ctypes.c_double,
+                                             ctypes.c_double, _dp, ctypes.c_long, _dp, _dp, _dp]
+            lib.fao_merge_states.restype = None
+            lib.fao_decode_splitkv.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                               ctypes.c_long, ctypes.c_long, ctypes.c_double, _ip]
+            lib.fao_decode_splitkv.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """Exact up-cast of a numpy array or a (CPU or CUDA) torch tensor to C-contiguous float64."""
+    if not isinstance(a, np.ndarray):  # torch tensor: go through float32, which holds bf16 exactly
+        import torch  # local: only when a tensor is handed in
+        t = a.detach()
+        if t.dtype in (torch.bfloat16, torch.float16):
+            t = t.float()
+        a = t.cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def attention(q, k, v, scale: float):
+    """Exact attention on [..., N, d] inputs; returns (O, LSE) as float64 arrays.
+
+    Leading dimensions (batch, heads) must agree between q, k and v; each head
+    is independent.  LSE has shape [..., Nq].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim < 2 or k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+        raise ValueError("shape mismatch")
+    lead = q.shape[:-2]
+    nq, d = q.shape[-2:]
+    nk = k.shape[-2]
+    bh = int(np.prod(lead)) if lead else 1
+    o = np.empty_like(q)
+    lse = np.empty(lead + (nq,), dtype=np.float64)
+    _check(_load().fao_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), 1, bh, nq, nk, d,
+                                 float(scale)), "attention")
+    return o, lse
+
+
+def partial_state(q, k, v, scale: float):
+    """(m, l, o) of one query q [d] over keys k/v [n, d] (n may be 0); o unnormalised."""
+    q, k, v = _f64(q), _f64(k).reshape(-1, len(q)), _f64(v)
+    n, d = k.shape[0], q.shape[0]
+    if v.size != n * d:
+        raise ValueError("v must be [n, d] like k")
+    v = v.reshape(n, d)
+    m, l = ctypes.c_double(), ctypes.c_double()
+    o = np.empty(d, dtype=np.float64)
+    _check(_load().fao_partial_state(_ptr(q), _ptr(k), _ptr(v), n, d, float(scale),
+                                     ctypes.byref(m), ctypes.byref(l), _ptr(o)), "partial_state")
+    return m.value, l.value, o
+
+
+def merge_states(a, b):
+    """Merge two partial states (m, l, o) -> (m, l, o)."""
+    (ma, la, oa), (mb, lb, ob) = a, b
+    oa, ob = _f64(oa), _f64(ob)
+    d = oa.shape[0]
+    m, l = ctypes.c_double(), ctypes.c_double()
+    o = np.empty(d, dtype=np.float64)
+    _load().fao_merge_states(float(ma), float(la), _ptr(oa), float(mb), float(lb), _ptr(ob), d,
+                             ctypes.byref(m), ctypes.byref(l), _ptr(o))
+    return m.value, l.value, o
+
+
+def finish(state) -> np.ndarray:
+    """Normalised output o / l of a partial state."""
+    _, l, o = state
+    return o / l
+
+
+def decode_splitkv(q, k, v, splits: int, scale: float, order=None):
+    """Split-KV attention of one query per head.
+
+    q [..., d] (or [..., 1, d]), k/v [..., Nk, d].  Keys are cut into `splits`
+    chunks of ceil(Nk/splits); chunk states are merged in `order` (a
+    permutation; None = index order).  Returns (O [..., d], LSE [...]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    lead = k.shape[:-2]
+    nk, d = k.shape[-2:]
+    q = q.reshape(lead + (d,))
+    bh = int(np.prod(lead)) if lead else 1
+    o = np.empty(lead + (d,), dtype=np.float64)
+    lse = np.empty(lead, dtype=np.float64)
+    ordp = None
+    if order is not None:
+        order = np.ascontiguousarray(order, dtype=np.int32)
+        if order.shape != (splits,):
+            raise ValueError("order must be a permutation of range(splits)")
+        ordp = order.ctypes.data_as(_ip)
+    _check(_load().fao_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), bh, nk, d,
+                                      int(splits), float(scale), ordp), "decode_splitkv")
+    return o, lse
