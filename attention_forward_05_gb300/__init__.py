@@ -1,0 +1,205 @@
+"""attention_forward_05_gb300 -- Python binding of libfa (FlashAttention forward for GB300).
+
+This module only marshals arguments: it checks tensors, takes their device
+pointers and the current CUDA stream, and calls the C ABI of ``libfa.so``
+(declared in ``include/fa.h``).  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback.  If the library is missing or
+fails to load, importing the binding's entry points raises.
+
+Entry points (same names as the C ABI):
+  fa_fwd(q, k, v, scale=None, o=None, lse=None, with_lse=True) -> (o, lse)
+  fa_decode_splitkv(q, k, v, splits, o=None) -> o
+  fa_decode_splitkv_ex(q, k, v, splits, scale=None, workspace=None, merge_order=None, with_lse=False)
+  fa_decode_workspace_bytes(B, H, d, splits)
+  fa_check_device_error()
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build
+
+FA_FP32, FA_BF16 = 0, 1
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {status_string(status)} ({status})"
+        if status == FA_ERR_CUDA:
+            L = lib()
+            msg += f": {L.fa_last_cuda_error_string().decode()} [{L.fa_last_cuda_error()}]"
+        super().__init__(msg)
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfa.so (built first if stale).  Raises if it cannot be built or loaded."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if _build.is_stale() else _build.LIB
+            L = ctypes.CDLL(path)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+            L.fa_fwd.restype = i
+            L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+            L.fa_decode_splitkv.restype = i
+            L.fa_decode_splitkv_ex.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp, vp, vp]
+            L.fa_decode_splitkv_ex.restype = i
+            L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
+            L.fa_decode_workspace_bytes.restype = sz
+            L.fa_check_device_error.argtypes = []
+            L.fa_check_device_error.restype = i
+            L.fa_status_string.argtypes = [i]
+            L.fa_status_string.restype = ctypes.c_char_p
+            L.fa_debug_set_fault.argtypes = [i]
+            L.fa_debug_set_fault.restype = i
+            L.fa_last_cuda_error.argtypes = []
+            L.fa_last_cuda_error.restype = i
+            L.fa_last_cuda_error_string.argtypes = []
+            L.fa_last_cuda_error_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _need_cuda_contig(name: str, t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+           o: torch.Tensor | None = None, lse: torch.Tensor | None = None, with_lse: bool = True,
+           stream=None):
+    """Exact attention softmax(q k^T * scale) v over [B, H, N, d] tensors; returns (o, lse or None)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(n, t)
+    if q.dim() != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d], k/v [B,H,Nk,d] expected")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    _need_cuda_contig("o", o)
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must match q")
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    if lse is not None:
+        _need_cuda_contig("lse", lse)
+        if lse.shape != (B, H, Nq) or lse.dtype != torch.float32:
+            raise ValueError("lse must be fp32 [B,H,Nq]")
+    st = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                      lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, float(scale),
+                      _dtype_code(q), _stream_handle(stream))
+    _check(st, "fa_fwd")
+    return o, lse
+
+
+def _decode_shapes(q, k, v):
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(n, t)
+    if k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("k/v [B,H,Nk,d] expected")
+    B, H, Nk, d = k.shape
+    if q.numel() != B * H * d:
+        raise ValueError("q must hold B*H*d elements ([B,H,d] or [B,H,1,d])")
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise TypeError("decode takes bf16 q, k, v")
+    return B, H, Nk, d
+
+
+def fa_decode_splitkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, splits: int,
+                      o: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Split-KV decode with scale 1/sqrt(d); returns o [B, H, d] bf16."""
+    B, H, Nk, d = _decode_shapes(q, k, v)
+    if o is None:
+        o = torch.empty((B, H, d), device=q.device, dtype=torch.bfloat16)
+    _need_cuda_contig("o", o)
+    st = lib().fa_decode_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Nk, d,
+                                 int(splits), _stream_handle(stream))
+    _check(st, "fa_decode_splitkv")
+    return o
+
+
+def fa_decode_workspace_bytes(B: int, H: int, d: int, splits: int) -> int:
+    return int(lib().fa_decode_workspace_bytes(B, H, d, splits))
+
+
+def fa_decode_splitkv_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, splits: int,
+                         scale: float | None = None, workspace: torch.Tensor | None = None,
+                         merge_order: torch.Tensor | None = None, with_lse: bool = False,
+                         o: torch.Tensor | None = None, stream=None):
+    """Split-KV decode with explicit scale, caller workspace, merge order and LSE; returns (o, lse)."""
+    B, H, Nk, d = _decode_shapes(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, d), device=q.device, dtype=torch.bfloat16)
+    _need_cuda_contig("o", o)
+    lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if with_lse else None
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need_cuda_contig("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    ord_ptr = None
+    if merge_order is not None:
+        _need_cuda_contig("merge_order", merge_order)
+        if merge_order.dtype != torch.int32 or merge_order.numel() != splits:
+            raise ValueError("merge_order must be int32 [splits]")
+        ord_ptr = merge_order.data_ptr()
+    st = lib().fa_decode_splitkv_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Nk, d,
+                                    int(splits), float(scale), ws_ptr, ws_bytes, ord_ptr,
+                                    lse.data_ptr() if lse is not None else None, _stream_handle(stream))
+    _check(st, "fa_decode_splitkv_ex")
+    return o, lse
+
+
+def fa_check_device_error() -> int:
+    """Synchronises the current device and returns (and clears) the library's device status."""
+    return int(lib().fa_check_device_error())
+
+
+def fa_debug_set_fault(mode: int) -> int:
+    """Test only: arm (1) or disarm (0) the load-warp fault of the next fa_fwd launch."""
+    return int(lib().fa_debug_set_fault(int(mode)))

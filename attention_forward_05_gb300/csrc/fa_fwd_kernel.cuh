@@ -1,0 +1,476 @@
+// fa_fwd_kernel.cuh -- fused FlashAttention forward for sm_103a.
+//
+// Sources (web pages, cited by title and section):
+//   [T1] "FlashAttention 简化版：Tiling + Online Softmax" (forceinjection.github.io)
+//   [T3] "CS349E 第 11 讲 01_online_softmax.py" (semidirectx.com)
+//
+// Algorithm: Q-outer / KV-inner tiling with the online-softmax recurrence
+// ([T1] §2.3 and §3.1): for each key tile j the row maximum m, the running sum
+// l and the unnormalised output O are updated with alpha = exp(m_old - m_new);
+// O is divided by l once after the last tile ([T3] demo 3, deferred
+// normalisation).  The score tile lives only in tensor memory.
+//
+// One CTA owns NQT query tiles of 128 rows of one (batch, head) and walks all
+// key tiles of Bc rows.  Warp roles:
+//   warps 0 .. 4*NQT-1   softmax warpgroup t = warp/4 owns query tile t; thread
+//                        = one query row (TMEM lane).  It reads S_t from TMEM,
+//                        updates m and l, rescales O_t in TMEM when needed,
+//                        writes P_t (bf16, or fp32 for the TF32 path) back over
+//                        S_t, and finally writes O_t / l and the LSE.
+//   warp 4*NQT           TMA producer: Q once, then K_j and V_j into a ring of
+//                        STAGES shared-memory slots (mbarrier full/empty pairs).
+//   warp 4*NQT+1         MMA issuer (one thread): S_t = Q_t K_j^T (both operands
+//                        in shared memory, K-major, 128-byte swizzle) and
+//                        O_t += P_t V_j (P from tensor memory, V MN-major).
+// With NQT = 2 the two query tiles ping-pong: while warpgroup 0 does the
+// softmax of step j the tensor core computes tile 1's products, and vice versa
+// ([T3] demo 3 remark on FA3-style ping-pong of softmax and MMA).
+//
+// Lazy rescale: a row's reference maximum m_ref only moves when the new
+// maximum exceeds it by more than tau (log2 units).  P = 2^(t - m_ref) then
+// stays below 2^tau, and since O and l share m_ref, O / l is unchanged; with
+// tau = 0 this is exactly the per-step correction of [T1] §2.3.
+#pragma once
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+template <typename T, int D_, int BC_, int NQT_, int STAGES_>
+struct FwdCfg {
+  using Elem = T;
+  static constexpr int D = D_;
+  static constexpr int BC = BC_;
+  static constexpr int NQT = NQT_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int BR = 128;
+  static constexpr int ESZ = static_cast<int>(sizeof(T));
+  static constexpr bool TF32 = (ESZ == 4);
+  static constexpr uint32_t FMT = TF32 ? 2u : 1u;
+  static constexpr int CHUNK = 128 / ESZ;  // elements per 128-byte swizzled row segment
+  static constexpr int NCH = D / CHUNK;    // segments per row
+  static constexpr int Q_CH_BYTES = BR * 128;
+  static constexpr int KV_CH_BYTES = BC * 128;
+  static constexpr int Q_BYTES = NCH * Q_CH_BYTES;
+  static constexpr int KV_BYTES = NCH * KV_CH_BYTES;
+  // V as the B operand of O += P V.  bf16: V tiles [Bc keys][D] are MN-major.  tf32 MMAs accept only
+  // K-major operands, so the fp32 path reads a key-major copy V^T [D][Nk] and its tiles are [D rows][Bc].
+  static constexpr bool V_KMAJOR = TF32;
+  static constexpr int NCH_V = V_KMAJOR ? BC / CHUNK : NCH;
+  static constexpr int V_CH_BYTES = V_KMAJOR ? D * 128 : KV_CH_BYTES;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQT * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT], drain
+  static constexpr int NBAR = 1 + 4 * STAGES + 3 * NQT + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr int MMA_K = 32 / ESZ;                  // K of one tcgen05.mma (32 bytes)
+  static constexpr int O_COL0 = NQT * BC;                 // TMEM: S_t at t*BC, O_t at O_COL0 + t*D
+  static constexpr int TMEM_NEED = NQT * (BC + D);
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
+                                   : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int P_COLS = BC * ESZ / 4;  // 32-bit TMEM columns of one P row
+  static constexpr int P_COLS_PER_K = MMA_K * ESZ / 4;
+  static constexpr int NWARPS = 4 * NQT + 2;
+  static constexpr int NTHREADS = 32 * NWARPS;
+  static constexpr int LOAD_WARP = 4 * NQT;
+  static constexpr int MMA_WARP = 4 * NQT + 1;
+  static_assert(D % CHUNK == 0, "head dim must be a whole number of 128-byte segments");
+  static_assert(BC % 32 == 0 && BC >= 32 && BC <= 256, "key tile");
+  static_assert(TMEM_NEED <= 512, "tensor memory");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+struct FwdParams {
+  void* o;
+  float* lse;
+  int* err;
+  int Nq, Nk, n_qblk;
+  float c, tau;
+  int fault;
+};
+
+// wait-site identifiers recorded with a timeout
+enum : int { W_Q = 1, W_KF, W_VF, W_KE, W_VE, W_SF, W_PF, W_OD, W_DRAIN_MMA, W_DRAIN_K, W_DRAIN_V };
+
+template <class C>
+__global__ void __launch_bounds__(C::NTHREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int qb = blockIdx.x % p.n_qblk;
+  const int bh = blockIdx.x / p.n_qblk;
+  const int q0 = qb * C::BR * C::NQT;
+  const int T = (p.Nk + C::BC - 1) / C::BC;
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t bar_q = bar0;
+  auto bar_kf = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_vf = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
+  auto bar_ke = [&](int s) { return bar0 + 8u * (1 + 2 * C::STAGES + s); };
+  auto bar_ve = [&](int s) { return bar0 + 8u * (1 + 3 * C::STAGES + s); };
+  auto bar_sf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + t); };
+  auto bar_pf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + C::NQT + t); };
+  auto bar_od = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 2 * C::NQT + t); };
+  const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_kf(s), 1);
+      mbar_init(bar_vf(s), 1);
+      mbar_init(bar_ke(s), 1);
+      mbar_init(bar_ve(s), 1);
+    }
+    for (int t = 0; t < C::NQT; ++t) {
+      mbar_init(bar_sf(t), 1);
+      mbar_init(bar_pf(t), 4);  // one arrive per softmax warp
+      mbar_init(bar_od(t), 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::LOAD_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int nk_issued[C::STAGES], nv_issued[C::STAGES];
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) nk_issued[s] = nv_issued[s] = 0;
+      mbar_expect_tx(bar_q, C::NQT * C::Q_BYTES);
+#pragma unroll
+      for (int t = 0; t < C::NQT; ++t)
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sbase + C::OFF_Q + t * C::Q_BYTES + c * C::Q_CH_BYTES, &tm_q, bar_q, c * C::CHUNK,
+                      q0 + t * C::BR, bh);
+      for (int j = 0; j < T; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = ((j / C::STAGES) & 1) ^ 1;
+        if (!mbar_wait(bar_ke(s), ph, abort_flag, p.err, W_KE)) break;
+        if (!(p.fault == 1 && j == 0)) {
+          mbar_expect_tx(bar_kf(s), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sbase + C::OFF_K + s * C::KV_BYTES + c * C::KV_CH_BYTES, &tm_k, bar_kf(s),
+                        c * C::CHUNK, j * C::BC, bh);
+          ++nk_issued[s];
+        }
+        if (!mbar_wait(bar_ve(s), ph, abort_flag, p.err, W_VE)) break;
+        mbar_expect_tx(bar_vf(s), C::KV_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCH_V; ++c) {
+          if constexpr (C::V_KMAJOR)
+            tma_load_3d(sbase + C::OFF_V + s * C::KV_BYTES + c * C::V_CH_BYTES, &tm_v, bar_vf(s),
+                        j * C::BC + c * C::CHUNK, 0, bh);
+          else
+            tma_load_3d(sbase + C::OFF_V + s * C::KV_BYTES + c * C::V_CH_BYTES, &tm_v, bar_vf(s), c * C::CHUNK,
+                        j * C::BC, bh);
+        }
+        ++nv_issued[s];
+      }
+      // Drain: every copy this thread issued must land before the CTA exits.
+      mbar_wait_drain(bar_q, 0, p.err, W_DRAIN_K);
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (nk_issued[s] > 0) mbar_wait_drain(bar_kf(s), (nk_issued[s] - 1) & 1, p.err, W_DRAIN_K);
+        if (nv_issued[s] > 0) mbar_wait_drain(bar_vf(s), (nv_issued[s] - 1) & 1, p.err, W_DRAIN_V);
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc(C::FMT, C::BR, C::BC, 0, 0);
+      constexpr uint32_t idesc_pv = make_idesc(C::FMT, C::BR, C::D, 0, C::V_KMAJOR ? 0 : 1);
+      auto issue_qk = [&](int t, int s) {
+        const uint32_t d_tmem = tmem + t * C::BC;
+#pragma unroll
+        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+          const int e = kk * C::MMA_K;
+          const uint32_t off = (e % C::CHUNK) * C::ESZ;  // byte offset inside the 128-byte segment
+          const uint32_t qa = sbase + C::OFF_Q + t * C::Q_BYTES + (e / C::CHUNK) * C::Q_CH_BYTES + off;
+          const uint32_t kb = sbase + C::OFF_K + s * C::KV_BYTES + (e / C::CHUNK) * C::KV_CH_BYTES + off;
+          mma_ss<C::TF32>(d_tmem, sdesc_sw128(qa, 16, 1024), sdesc_sw128(kb, 16, 1024), idesc_qk, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int s, bool acc) {
+        const uint32_t d_tmem = tmem + C::O_COL0 + t * C::D;
+        const uint32_t a_tmem = tmem + t * C::BC;
+#pragma unroll
+        for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
+          uint64_t vdesc;
+          if constexpr (C::V_KMAJOR) {  // [D rows][Bc keys]: step along keys inside 128-byte segments
+            const int e = kk * C::MMA_K;
+            vdesc = sdesc_sw128(sbase + C::OFF_V + s * C::KV_BYTES + (e / C::CHUNK) * C::V_CH_BYTES +
+                                    (e % C::CHUNK) * C::ESZ,
+                                16, 1024);
+          } else {  // [Bc keys][D]: MN-major, 8-key groups 1024 B apart, 64-column segments LBO apart
+            vdesc = sdesc_sw128(sbase + C::OFF_V + s * C::KV_BYTES + kk * C::MMA_K * 128, C::V_CH_BYTES, 1024);
+          }
+          mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_K, vdesc, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, W_Q) && mbar_wait(bar_kf(0), 0, abort_flag, p.err, W_KF);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < C::NQT; ++t) {
+          issue_qk(t, 0);
+          mma_commit(bar_sf(t));
+        }
+        mma_commit(bar_ke(0));
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j % C::STAGES;
+        const int j1 = j + 1;
+        const int s1 = j1 % C::STAGES;
+        ok = mbar_wait(bar_vf(s), (j / C::STAGES) & 1, abort_flag, p.err, W_VF);
+        if (!ok) break;
+#pragma unroll
+        for (int t = 0; t < C::NQT; ++t) {
+          ok = mbar_wait(bar_pf(t), j & 1, abort_flag, p.err, W_PF);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          if (t == C::NQT - 1) mma_commit(bar_ve(s));
+          if (j1 < T) {
+            if (t == 0) {
+              ok = mbar_wait(bar_kf(s1), (j1 / C::STAGES) & 1, abort_flag, p.err, W_KF);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_qk(t, s1);
+            mma_commit(bar_sf(t));
+            if (t == C::NQT - 1) mma_commit(bar_ke(s1));
+          } else {
+            mma_commit(bar_od(t));
+          }
+        }
+      }
+      // Drain: all MMAs issued above complete before tensor memory is freed.
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0, p.err, W_DRAIN_MMA);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * C::BC;
+    const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::D;
+    const float c = p.c;
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      ok = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[C::BC / 32][32];
+#pragma unroll
+      for (int i = 0; i < C::BC / 32; ++i) tmem_ld32(tS + i * 32, sr[i]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < C::BC / 32; ++i) reg_fence(sr[i]);
+
+      const int valid = p.Nk - j * C::BC;  // >= 1
+      if (valid < C::BC) {                  // ragged last tile: repeat column 0 so max/min ignore the pad
+        const uint32_t s0 = sr[0][0];
+#pragma unroll
+        for (int i = 0; i < C::BC / 32; ++i)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (i * 32 + e >= valid) sr[i][e] = s0;
+      }
+      // row extreme of the raw scores (max for scale >= 0, min for scale < 0)
+      float mx[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mx[e] = __uint_as_float(sr[0][e]);
+      if (c >= 0.f) {
+#pragma unroll
+        for (int i = 0; i < C::BC / 32; ++i)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sr[i][e]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < C::BC / 32; ++i)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx[e & 3] = fminf(mx[e & 3], __uint_as_float(sr[i][e]));
+      }
+      const float m_tile = (c >= 0.f ? fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]))
+                                     : fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3]))) * c;
+      const float m_new = fmaxf(m_ref, m_tile);
+      const bool need = m_new > m_ref + p.tau;  // always true on the first tile (m_ref = -inf)
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
+        m_ref = m_new;
+      }
+      // correction of O_t (its last update, P V of step j-1, completed before S_t of step j did)
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int cc = 0; cc < C::D / 32; ++cc) {
+          uint32_t orr[32];
+          tmem_ld32(tO + cc * 32, orr);
+          tmem_wait_ld();
+          reg_fence(orr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+          tmem_st32(tO + cc * 32, orr);
+        }
+      }
+      // P = 2^(s*c - m_ref), row sum in fp32
+      const float neg_m = -m_ref;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      if (valid >= C::BC) {
+#pragma unroll
+        for (int i = 0; i < C::BC / 32; ++i)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float pv = ex2_approx(fmaf(__uint_as_float(sr[i][e]), c, neg_m));
+            rs[e & 3] += pv;
+            sr[i][e] = __float_as_uint(pv);
+          }
+      } else {  // ragged last tile: padded key columns get P = 0
+#pragma unroll
+        for (int i = 0; i < C::BC / 32; ++i)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float pv = (i * 32 + e < valid) ? ex2_approx(fmaf(__uint_as_float(sr[i][e]), c, neg_m)) : 0.f;
+            rs[e & 3] += pv;
+            sr[i][e] = __float_as_uint(pv);
+          }
+      }
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      if constexpr (C::TF32) {  // round P to the nearest tf32 (the MMA would truncate)
+#pragma unroll
+        for (int i = 0; i < C::BC / 32; ++i) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(sr[i][e]) : "f"(__uint_as_float(sr[i][e])));
+          tmem_st32(tS + i * 32, sr[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < C::P_COLS / 32; ++i) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = i * 64 + 2 * e;  // two bf16 per 32-bit column, even element in the low half
+            pk[e] = pack_bf16x2(__uint_as_float(sr[col / 32][col % 32]),
+                                __uint_as_float(sr[(col + 1) / 32][(col + 1) % 32]));
+          }
+          tmem_st32(tS + i * 32, pk);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pf(t));
+    }
+    // ---------------------------------------------------------- epilogue: O / l, LSE
+    if (ok) {
+      ok = mbar_wait(bar_od(t), 0, abort_flag, p.err, W_OD);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const int qrow = q0 + t * C::BR + row;
+      const bool in_range = qrow < p.Nq;
+      uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * C::ESZ);
+#pragma unroll
+      for (int cc = 0; cc < C::D / 32; ++cc) {
+        uint32_t orr[32];
+        tmem_ld32(tO + cc * 32, orr);
+        tmem_wait_ld();
+        reg_fence(orr);
+        if (in_range) {
+          if constexpr (C::TF32) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32 * 4);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              uint4 w;
+              w.x = __float_as_uint(__uint_as_float(orr[4 * v4 + 0]) * inv_l);
+              w.y = __float_as_uint(__uint_as_float(orr[4 * v4 + 1]) * inv_l);
+              w.z = __float_as_uint(__uint_as_float(orr[4 * v4 + 2]) * inv_l);
+              w.w = __float_as_uint(__uint_as_float(orr[4 * v4 + 3]) * inv_l);
+              dst[v4] = w;
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32 * 2);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(orr[8 * v4 + 0]) * inv_l, __uint_as_float(orr[8 * v4 + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(orr[8 * v4 + 2]) * inv_l, __uint_as_float(orr[8 * v4 + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(orr[8 * v4 + 4]) * inv_l, __uint_as_float(orr[8 * v4 + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(orr[8 * v4 + 6]) * inv_l, __uint_as_float(orr[8 * v4 + 7]) * inv_l);
+              dst[v4] = w;
+            }
+          }
+        }
+      }
+      if (p.lse != nullptr && in_range)
+        p.lse[static_cast<size_t>(bh) * p.Nq + qrow] = (m_ref + log2f(l)) * 0.6931471805599453f;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::LOAD_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <class C>
+cudaError_t launch_fwd(const FwdLaunch& a) {
+  // per device and cheap: set on every launch so any current device is covered
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  FwdParams p;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.err = a.err;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.n_qblk = (a.Nq + C::BR * C::NQT - 1) / (C::BR * C::NQT);
+  p.c = a.c;
+  p.tau = a.tau;
+  p.fault = a.fault;
+  const long long grid = static_cast<long long>(p.n_qblk) * a.BH;
+  if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  fa_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream>>>(*a.tm_q, *a.tm_k,
+                                                                                        *a.tm_v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

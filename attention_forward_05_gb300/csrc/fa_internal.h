@@ -1,0 +1,58 @@
+// fa_internal.h -- launch interfaces between the C ABI (fa_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct FwdLaunch {
+  const CUtensorMap* tm_q;  // 3-D maps over [B*H, N, d] (innermost d), 128-byte swizzle
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  void* o;                  // [B, H, Nq, d], same dtype as the inputs
+  float* lse;               // [B, H, Nq] or nullptr
+  int* err;                 // device error word
+  int BH, Nq, Nk;
+  float c;                  // scale * log2(e)
+  float tau;                // lazy-rescale threshold in log2 units (0 = rescale whenever m grows)
+  int fault;                // test-only fault injection mode (0 = none)
+  cudaStream_t stream;
+};
+
+// Tile geometry the tensor maps must be encoded with, per instantiation.
+struct FwdGeometry {
+  int box_cols;  // elements per 128-byte row segment (64 bf16, 32 fp32)
+  int q_rows;    // rows per Q box (128)
+  int kv_rows;   // rows per K box (the KV tile, Bc)
+  int v_kmajor;  // 1: V is read from a key-major copy [BH, d, Nk_pad] with boxes (32 keys, d rows)
+};
+
+FwdGeometry fwd_geometry(int dtype_is_bf16, int d);
+
+// fp32 prep pass: qr = tf32(q), kr = tf32(k) (round to nearest), and the key-major copy
+// vt[bh][c][j] = tf32(v[bh][j][c]) for j < Nk, 0 for Nk <= j < Nk_pad.
+cudaError_t launch_prep_fp32(const float* q, const float* k, const float* v, float* qr, float* kr, float* vt,
+                             int BH, int Nq, int Nk, int Nk_pad, int d, cudaStream_t stream);
+cudaError_t launch_fwd_bf16_d64(const FwdLaunch& a);
+cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a);
+cudaError_t launch_fwd_fp32_d64(const FwdLaunch& a);
+cudaError_t launch_fwd_fp32_d128(const FwdLaunch& a);
+
+struct DecodeLaunch {
+  const void* q;            // [BH, d] bf16
+  const void* k;            // [BH, Nk, d] bf16
+  const void* v;
+  void* o;                  // [BH, d] bf16
+  float* lse;               // [BH] or nullptr
+  float* ws;                // workspace: m [BH*splits], l [BH*splits], o [BH*splits*d]
+  const int* order;         // [splits] or nullptr
+  int BH, Nk, d, splits;
+  float c;                  // scale * log2(e)
+  cudaStream_t stream;
+};
+
+cudaError_t launch_decode(const DecodeLaunch& a);
+
+}  // namespace fa

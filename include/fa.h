@@ -1,0 +1,141 @@
+/*
+ * fa.h -- C ABI of libfa: fused FlashAttention forward and split-KV decode
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [T1] "FlashAttention 简化版：Tiling + Online Softmax" (forceinjection.github.io)
+ *   [T2] "Flash Attention 代码填空 (Level 2-3)" (boots-coder.github.io, LLM-101-CN)
+ *   [T3] "CS349E 第 11 讲 01_online_softmax.py" (semidirectx.com)
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous row-major [B, H, N, d] (d fastest).  Decode q and
+ *     o are [B, H, d] (one query per head).  LSE is fp32 [B, H, Nq].
+ *   - Every pointer is a DEVICE pointer owned by the caller; base addresses
+ *     must be 16-byte aligned.  The library never frees caller memory and
+ *     keeps no pointer after a call returns.
+ *   - Calls are asynchronous: they validate, enqueue kernels on `stream`
+ *     (NULL = the legacy default stream) and return.  A return of FA_OK means
+ *     the work was enqueued; timeouts detected on the device are reported
+ *     later by fa_check_device_error().
+ *   - Arguments are validated before anything is launched; on any error
+ *     nothing is enqueued.  No call prints or exits.
+ *   - Calls are reentrant and may be made from several host threads.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so this header needs no CUDA header. */
+struct CUstream_st;
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum { FA_FP32 = 0, FA_BF16 = 1 } fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* NULL or misaligned pointer, non-positive size, overflow, bad scale */
+    FA_ERR_UNSUPPORTED = 2, /* valid but unsupported: head dim not 64/128, dtype, device not sm_103 */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, allocation, tensor map) */
+    FA_ERR_TIMEOUT = 4      /* a device-side wait ran past its limit (from fa_check_device_error) */
+} fa_status;
+
+/*
+ * fa_fwd -- exact attention O = softmax(Q K^T * scale) V, computed tile by
+ * tile with the online-softmax recurrence so the Nq x Nk score matrix never
+ * reaches device memory ([T1] §2.3, §3.1; [T3] attn_row_1pass).  For each
+ * query row the running maximum m, running sum l and unnormalised O are
+ * updated per key tile with correction alpha = exp(m_old - m_new); O is
+ * divided by l once at the end ([T3] demo 3, deferred normalisation).
+ *
+ *   q   [B, H, Nq, d]  in dtype       k, v [B, H, Nk, d] in dtype
+ *   o   [B, H, Nq, d]  out, dtype     lse  [B, H, Nq] fp32 out, or NULL
+ *   lse = m + ln(l) in natural log, in units of scaled scores ([T3] demo 2).
+ *   dtype FA_BF16: bf16 operands, fp32 accumulation, P rounded to bf16 for P V.
+ *   dtype FA_FP32: fp32 operands multiplied as TF32, P kept at TF32.  A prep
+ *     pass first writes tf32-rounded (nearest) copies of Q and K and a
+ *     key-major tf32 copy of V (tf32 tensor-core operands must be K-major)
+ *     into a stream-ordered workspace of about 4*B*H*d*(Nq + 2*Nk) bytes
+ *     (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *   d must be 64 or 128; Nq, Nk >= 1 (ragged tails are masked); B, H >= 1;
+ *   scale must be finite (1/sqrt(d) is the usual value; 1 reproduces [T4]-style
+ *   unscaled scores).  Returns FA_OK or an fa_status code.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int Nq, int Nk, int d, float scale, int dtype,
+           fa_stream_t stream);
+
+/*
+ * fa_decode_splitkv -- attention of one bf16 query per head over Nk keys,
+ * split into `splits` chunks of ceil(Nk/splits) keys processed in parallel
+ * (flash-decoding); each chunk yields a partial state (m, l, o) with o
+ * unnormalised, and a second kernel merges the states ([T3] demo 2: the merge
+ * is associative and commutative) and writes O = o / l as bf16.
+ *
+ *   q [B, H, d] bf16, k/v [B, H, Nk, d] bf16, o [B, H, d] bf16 out.
+ *   scale is fixed at 1/sqrt(d).  1 <= splits <= Nk; d in {64, 128}.
+ *   The fp32 workspace for the partial states is taken stream-ordered
+ *   (cudaMallocAsync / cudaFreeAsync on `stream`).
+ */
+int fa_decode_splitkv(const void* q, const void* k, const void* v, void* o,
+                      int B, int H, int Nk, int d, int splits,
+                      fa_stream_t stream);
+
+/*
+ * fa_decode_splitkv_ex -- fa_decode_splitkv with every option exposed.
+ *   scale        finite score scale.
+ *   workspace    device buffer of at least fa_decode_workspace_bytes(B, H, d,
+ *                splits) bytes, 16-byte aligned; NULL = allocate stream-ordered.
+ *   merge_order  device int32 [splits], a permutation of 0..splits-1 giving the
+ *                order in which chunk states are accumulated by the merge; NULL
+ *                = index order.  The result is the same up to rounding for
+ *                every order ([T3] demo 2).  Entries are validated on the
+ *                device; a non-permutation makes the merge write NaN outputs.
+ *   lse          fp32 [B, H] out (natural log, scaled-score units), or NULL.
+ */
+int fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o,
+                         int B, int H, int Nk, int d, int splits, float scale,
+                         void* workspace, size_t workspace_bytes,
+                         const int* merge_order, float* lse, fa_stream_t stream);
+
+/* Bytes of fp32 partial-state workspace fa_decode_splitkv_ex needs; 0 on bad arguments. */
+size_t fa_decode_workspace_bytes(int B, int H, int d, int splits);
+
+/*
+ * fa_check_device_error -- reads and clears the library's device error word
+ * on the current device (synchronises that device).  Returns FA_OK, or
+ * FA_ERR_TIMEOUT if a kernel gave up on a wait since the last check (its
+ * outputs are then undefined), or FA_ERR_CUDA if the read itself failed.
+ */
+int fa_check_device_error(void);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(int status);
+
+/*
+ * fa_last_cuda_error -- the CUDA error behind the calling host thread's last
+ * FA_ERR_CUDA (a cudaError_t value, or 100000 + a CUresult from tensor-map
+ * encoding); 0 if none.  fa_last_cuda_error_string gives its static text.
+ */
+int fa_last_cuda_error(void);
+const char* fa_last_cuda_error_string(void);
+
+/*
+ * fa_debug_set_fault -- TEST ONLY.  Arms a host-side fault for the next
+ * fa_fwd launch on this process: mode 1 makes the kernel's load warp skip
+ * its first key-tile copy (and its expected-byte count), so the consumer's
+ * bounded wait runs out, the kernel abandons its work, records
+ * FA_ERR_TIMEOUT and returns.  mode 0 disarms.  Returns FA_OK or
+ * FA_ERR_INVALID_ARG.
+ */
+int fa_debug_set_fault(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,128 @@
+"""Comparison helpers and tolerances for the GPU-vs-oracle parity tests.
+
+Tolerances (absolute, on outputs of O(1) inputs), fixed by the build's target
+and consistent with the pages' precision study ("CS349E 第 11 讲
+01_online_softmax.py", demo 4: P in bf16 gives ~1e-3 relative error with
+fp32 m, l and accumulators):
+  fp32 inputs (TF32 products):  max |dO| <= 2e-3
+  bf16 inputs:                  max |dO| <= 1.5e-2 and mean |dO| <= 2e-3
+  LSE (both):                   max |dLSE| <= 1e-3
+The oracle always runs on the exact bytes the GPU saw (bf16 up-cast exactly).
+
+Two readings make these bounds attainable at the edges, both derived from the
+arithmetic rather than tuned:
+  * bf16 output: O is stored in bf16, so even a correctly rounded output is up
+    to half a bf16 step from the exact value (0.0156 once |O| >= 4, which
+    happens with peaked scores where O is close to a single V row).  The
+    1.5e-2 bound is applied to the error beyond that half step.
+  * fp32 inputs: Q and K are rounded to tf32 (unit roundoff u = 2^-11) before
+    the tensor core multiplies them, so a score can be off by up to
+    2u |scale| sum_i |q_i k_i|; LSE is a softmax-weighted mean of scores, so
+    its error is below the largest such score bound.  With few keys nothing
+    averages out, and the LSE bound is max(1e-3, that bound).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TOL = {
+    "fp32": dict(max_o=2e-3, mean_o=None, lse=1e-3),
+    "bf16": dict(max_o=1.5e-2, mean_o=2e-3, lse=1e-3),
+}
+
+
+def dtype_name(t: torch.Tensor) -> str:
+    return "bf16" if t.dtype == torch.bfloat16 else "fp32"
+
+
+def sample_rows(Nq: int, n_random: int, seed: int, tile: int = 128, n_tiles: int = 12) -> np.ndarray:
+    """Seeded rows: first and last row of the first two, the last, and `n_tiles` random 128-row
+    query tiles, plus `n_random` random rows."""
+    rng = np.random.default_rng(seed)
+    n_t = (Nq + tile - 1) // tile
+    tiles = {0, min(1, n_t - 1), n_t - 1}
+    tiles.update(rng.choice(n_t, size=min(n_tiles, n_t), replace=False).tolist())
+    rows = set()
+    for t in tiles:
+        rows.add(t * tile)
+        rows.add(min(Nq - 1, t * tile + tile - 1))
+    rows.update(rng.choice(Nq, size=min(n_random, Nq), replace=False).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_fwd(q, k, v, o, lse, scale: float, rows=None, name: str = "") -> dict:
+    """Compares GPU outputs (o, lse) with the oracle on all rows or on `rows`; asserts the tolerances."""
+    dt = dtype_name(q)
+    if rows is None:
+        qs, og, lg = q, o, lse
+    else:
+        idx = torch.as_tensor(rows, device=q.device)
+        qs, og = q[:, :, idx], o[:, :, idx]
+        lg = lse[:, :, idx] if lse is not None else None
+    ref_o, ref_lse = oracle.attention(qs, k, v, scale)
+    got = og.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all(), f"{name}: non-finite output"
+    err = np.abs(got - ref_o)
+    res = dict(max_o=float(err.max()), mean_o=float(err.mean()))
+    tol = TOL[dt]
+    beyond = err - bf16_half_step(ref_o) if dt == "bf16" else err
+    res["max_o_beyond_format"] = float(beyond.max())
+    assert res["max_o_beyond_format"] <= tol["max_o"], \
+        f"{name}: max|dO| {res['max_o']:.3e} ({res['max_o_beyond_format']:.3e} beyond bf16 rounding) > {tol['max_o']}"
+    if tol["mean_o"] is not None:
+        assert res["mean_o"] <= tol["mean_o"], f"{name}: mean|dO| {res['mean_o']:.3e} > {tol['mean_o']}"
+    if lg is not None:
+        le = np.abs(lg.cpu().numpy().astype(np.float64) - ref_lse)
+        res["lse"] = float(le.max())
+        lse_tol = np.full(le.shape, tol["lse"])
+        if dt == "fp32":
+            lse_tol = np.maximum(lse_tol, tf32_score_bound(qs, k, scale))
+        assert (le <= lse_tol).all(), f"{name}: max|dLSE| {res['lse']:.3e} above its bound"
+    return res
+
+
+def bf16_half_step(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers at |x| (8 significant bits): 2^(floor(log2|x|) - 8)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(ax)) - 8)
+
+
+def tf32_score_bound(q, k, scale: float) -> np.ndarray:
+    """Per query row, max over keys of 2u |scale| sum_i |q_i k_i| with u = 2^-11 (tf32 rounding of q and k)."""
+    qa = np.abs(q.float().cpu().numpy().astype(np.float64))
+    ka = np.abs(k.float().cpu().numpy().astype(np.float64))
+    per_key = np.einsum("bhqd,bhkd->bhqk", qa, ka)
+    return 2.0 * 2.0 ** -11 * abs(scale) * per_key.max(axis=-1) * 1.001
+
+
+def check_decode(q, k, v, o, lse, scale: float, splits: int, order=None, heads=None, name: str = "") -> dict:
+    """Decode outputs o [B,H,d] (and lse [B,H]) against the oracle's split-and-merge in the same order.
+
+    `heads` optionally restricts the check to a list of flat (b*H + h) indices.
+    """
+    B, H, Nk, d = k.shape
+    qf = q.reshape(B * H, d)
+    kf, vf = k.reshape(B * H, Nk, d), v.reshape(B * H, Nk, d)
+    of = o.reshape(B * H, d)
+    lf = lse.reshape(B * H) if lse is not None else None
+    if heads is not None:
+        idx = torch.as_tensor(heads, device=k.device)
+        qf, kf, vf, of = qf[idx], kf[idx], vf[idx], of[idx]
+        lf = lf[idx] if lf is not None else None
+    ref_o, ref_lse = oracle.decode_splitkv(qf, kf, vf, splits, scale, order)
+    got = of.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all(), f"{name}: non-finite output"
+    err = np.abs(got - ref_o)
+    res = dict(max_o=float(err.max()), mean_o=float(err.mean()))
+    tol = TOL["bf16"]
+    res["max_o_beyond_format"] = float((err - bf16_half_step(ref_o)).max())
+    assert res["max_o_beyond_format"] <= tol["max_o"], f"{name}: max|dO| {res['max_o']:.3e}"
+    assert res["mean_o"] <= tol["mean_o"], f"{name}: mean|dO| {res['mean_o']:.3e}"
+    if lf is not None:
+        le = np.abs(lf.cpu().numpy().astype(np.float64) - ref_lse)
+        res["lse"] = float(le.max())
+        assert res["lse"] <= tol["lse"], f"{name}: max|dLSE| {res['lse']:.3e}"
+    return res
