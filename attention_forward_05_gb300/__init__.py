@@ -195,6 +195,29 @@ def fa_decode_splitkv_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, spli
     return o, lse
 
 
+def fa_decode_splitkv_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, splits: int,
+                              o: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fa_decode_splitkv whose partial states use the library's fixed device scratch array.
+
+    For callers that may not allocate device memory during a call; the C
+    declaration in include/fa.h lists the size limit and the sharing rules
+    (calls that overlap on the GPU race on the one array).
+    """
+    B, H, Nk, d = _decode_shapes(q, k, v)
+    if o is None:
+        o = torch.empty((B, H, d), device=q.device, dtype=torch.bfloat16)
+    _need_cuda_contig("o", o)
+    L = lib()
+    fn = L.fa_decode_splitkv_noalloc
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    fn.restype = i
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Nk, d, int(splits),
+            _stream_handle(stream))
+    _check(st, "fa_decode_splitkv_noalloc")
+    return o
+
+
 def fa_check_device_error() -> int:
     """Synchronises the current device and returns (and clears) the library's device status."""
     return int(lib().fa_check_device_error())

@@ -1,6 +1,6 @@
 """Builds libfa.so in-tree with nvcc for sm_103a (no CMake, no torch extension machinery).
 
-The four translation units compile in parallel; the shared library links the
+The translation units compile in parallel; the shared library links the
 CUDA runtime statically, so it depends only on the driver.
 """
 from __future__ import annotations
@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_decode.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_decode.cu", "fa_decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -105,6 +105,36 @@ int fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o,
 /* Bytes of fp32 partial-state workspace fa_decode_splitkv_ex needs; 0 on bad arguments. */
 size_t fa_decode_workspace_bytes(int B, int H, int d, int splits);
 
+/* Size of the fixed device scratch array behind fa_decode_splitkv_noalloc. */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * fa_decode_splitkv_noalloc -- fa_decode_splitkv for callers that cannot
+ * allocate device memory during a call (for example serving processes that
+ * reserve nearly all device memory up front and forbid later allocations, or
+ * whose memory manager must own every allocation; cudaMalloc may also block
+ * on the device).  The pages have no counterpart: this is a deployment
+ * variant of the same split and merge kernels.
+ *
+ *   Arguments, layouts and results are those of fa_decode_splitkv (bf16,
+ *   scale 1/sqrt(d)).  The partial states live in a fixed array of
+ *   FA_DECODE_NOALLOC_SCRATCH_BYTES inside the library's device image, which
+ *   every GPU that loads the library holds until the process exits.  The call
+ *   allocates and frees nothing.
+ *   - FA_ERR_UNSUPPORTED if fa_decode_workspace_bytes(B, H, d, splits) exceeds
+ *     FA_DECODE_NOALLOC_SCRATCH_BYTES (nothing is launched).
+ *   - All calls share the array: calls whose kernels may overlap on the GPU
+ *     (unordered streams) race and must be ordered by the caller.  The array
+ *     keeps the previous call's contents; nothing needs clearing, since every
+ *     partial state is written before it is read.
+ *   - The first call on each device looks up the array's address
+ *     (cudaGetSymbolAddress, with that device current); make it before any
+ *     stream capture.
+ */
+int fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                              int B, int H, int Nk, int d, int splits,
+                              fa_stream_t stream);
+
 /*
  * fa_check_device_error -- reads and clears the library's device error word
  * on the current device (synchronises that device).  Returns FA_OK, or
