@@ -1,0 +1,52 @@
+"""Runs one kernel family on a named synthetic workload a few times (for profilers such as ncu).
+
+    python -m attention_forward_05_gb300.profile_run --workload mh_prefill --launches 2
+    python -m attention_forward_05_gb300.profile_run --workload decode --B 4 --launches 2
+
+The first launch is a warm-up; the process exits 0 after a device synchronise
+and a device-error check.  --B / --H override the workload's batch and heads
+(keeping the per-head shapes) so that a capture can stay small.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import sys
+
+import torch
+
+import attention_forward_05_gb300 as fa
+from attention_forward_05_gb300.inputs import WORKLOADS, merge_order, workload_inputs
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), required=True)
+    ap.add_argument("--launches", type=int, default=2)
+    ap.add_argument("--B", type=int, default=0)
+    ap.add_argument("--H", type=int, default=0)
+    a = ap.parse_args(argv)
+    w = WORKLOADS[a.workload]
+    if a.B:
+        w = dataclasses.replace(w, B=a.B)
+    if a.H:
+        w = dataclasses.replace(w, H=a.H)
+    dev = torch.device("cuda:0")
+    q, k, v = workload_inputs(w, device=dev)
+    torch.cuda.synchronize()
+    for _ in range(1 + a.launches):
+        if w.splits:
+            order = torch.as_tensor(merge_order(w.splits, w.order_seed), device=dev)
+            fa.fa_decode_splitkv_ex(q, k, v, w.splits, merge_order=order)
+        else:
+            fa.fa_fwd(q, k, v, scale=w.scale)
+    torch.cuda.synchronize()
+    if fa.fa_check_device_error() != fa.FA_OK:
+        print("device timeout", file=sys.stderr)
+        return 1
+    print(f"ok: {w.name} B={w.B} H={w.H} Nq={w.Nq} Nk={w.Nk} d={w.d} launches={a.launches}")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
