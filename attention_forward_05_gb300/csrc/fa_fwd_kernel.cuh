@@ -96,6 +96,70 @@ struct FwdParams {
 // wait-site identifiers recorded with a timeout
 enum : int { W_Q = 1, W_KF, W_VF, W_KE, W_VE, W_SF, W_PF, W_OD, W_DRAIN_MMA, W_DRAIN_K, W_DRAIN_V };
 
+// Row maximum (MAX) or minimum of the BC scores a thread holds: 4 independent
+// chains over groups of 8 elements, two new elements per 3-input max/min.
+template <class C, bool MAX>
+__device__ __forceinline__ float row_extreme(const uint32_t (&sr)[C::BC / 32][32]) {
+  static_assert(C::BC % 8 == 0, "groups of 8");
+  float a[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float x = __uint_as_float(sr[0][2 * u]), y = __uint_as_float(sr[0][2 * u + 1]);
+    a[u] = MAX ? fmaxf(x, y) : fminf(x, y);
+  }
+#pragma unroll
+  for (int g = 1; g < C::BC / 8; ++g)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = 8 * g + 2 * u;  // e and e + 1 lie in the same 32-column chunk
+      const float x = __uint_as_float(sr[e / 32][e % 32]), y = __uint_as_float(sr[e / 32][e % 32 + 1]);
+      a[u] = MAX ? max3f(a[u], x, y) : min3f(a[u], x, y);
+    }
+  return MAX ? max3f(a[0], a[1], fmaxf(a[2], a[3])) : min3f(a[0], a[1], fminf(a[2], a[3]));
+}
+
+// bf16 P: for 32-bit column q, elements 2q (low half) and 2q+1 (high half) of the row.
+template <class C, bool TAIL>
+__device__ __forceinline__ void softmax_p_bf16(const uint32_t (&sr)[C::BC / 32][32], uint32_t (&pk)[C::P_COLS / 32][32],
+                                               uint64_t c2, uint64_t negm2, int valid, uint64_t (&rs2)[2]) {
+#pragma unroll
+  for (int qc = 0; qc < C::P_COLS; ++qc) {
+    const int e0 = 2 * qc;
+    const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e0 / 32][e0 % 32]), __uint_as_float(sr[e0 / 32][e0 % 32 + 1])),
+                              c2, negm2);
+    float x0, x1;
+    f2_unpack_f(x, x0, x1);
+    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if (TAIL) {
+      if (e0 >= valid) p0 = 0.f;
+      if (e0 + 1 >= valid) p1 = 0.f;
+    }
+    rs2[qc & 1] = f2_add(rs2[qc & 1], f2_pack(p0, p1));
+    pk[qc / 32][qc % 32] = pack_bf16x2(p0, p1);
+  }
+}
+
+// tf32 P: one element per 32-bit column, rounded to the nearest tf32 (the MMA would truncate).
+template <class C, bool TAIL>
+__device__ __forceinline__ void softmax_p_tf32(uint32_t (&sr)[C::BC / 32][32], uint64_t c2, uint64_t negm2, int valid,
+                                               uint64_t (&rs2)[2]) {
+#pragma unroll
+  for (int e0 = 0; e0 < C::BC; e0 += 2) {
+    const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e0 / 32][e0 % 32]), __uint_as_float(sr[e0 / 32][e0 % 32 + 1])),
+                              c2, negm2);
+    float x0, x1;
+    f2_unpack_f(x, x0, x1);
+    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if (TAIL) {
+      if (e0 >= valid) p0 = 0.f;
+      if (e0 + 1 >= valid) p1 = 0.f;
+    }
+    rs2[(e0 >> 1) & 1] = f2_add(rs2[(e0 >> 1) & 1], f2_pack(p0, p1));
+    sr[e0 / 32][e0 % 32] = round_tf32_bits(p0);
+    sr[e0 / 32][e0 % 32 + 1] = round_tf32_bits(p1);
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::NTHREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -287,6 +351,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    const uint64_t c2 = f2_pack(c, c);
     for (int j = 0; j < T; ++j) {
       ok = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
       ok = __all_sync(0xffffffffu, ok);
@@ -308,23 +373,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           for (int e = 0; e < 32; ++e)
             if (i * 32 + e >= valid) sr[i][e] = s0;
       }
-      // row extreme of the raw scores (max for scale >= 0, min for scale < 0)
-      float mx[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) mx[e] = __uint_as_float(sr[0][e]);
-      if (c >= 0.f) {
-#pragma unroll
-        for (int i = 0; i < C::BC / 32; ++i)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sr[i][e]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < C::BC / 32; ++i)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx[e & 3] = fminf(mx[e & 3], __uint_as_float(sr[i][e]));
-      }
-      const float m_tile = (c >= 0.f ? fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]))
-                                     : fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3]))) * c;
+      // row extreme of the raw scores (max for scale >= 0, min for scale < 0), 3-input max/min
+      const float m_tile = (c >= 0.f ? row_extreme<C, true>(sr) : row_extreme<C, false>(sr)) * c;
       const float m_new = fmaxf(m_ref, m_tile);
       const bool need = m_new > m_ref + p.tau;  // always true on the first tile (m_ref = -inf)
       float alpha = 1.f;
@@ -332,8 +382,25 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         alpha = ex2_approx(m_ref - m_new);  // 0 on the first tile
         m_ref = m_new;
       }
-      // correction of O_t (its last update, P V of step j-1, completed before S_t of step j did)
+      // P = 2^(s*c - m_ref) (packed fp32 pairs), row sum in fp32, P written over S in TMEM
+      const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+      uint64_t rs2[2] = {0ull, 0ull};
+      if constexpr (C::TF32) {
+        if (valid >= C::BC) softmax_p_tf32<C, false>(sr, c2, negm2, valid, rs2);
+        else softmax_p_tf32<C, true>(sr, c2, negm2, valid, rs2);
+#pragma unroll
+        for (int i = 0; i < C::BC / 32; ++i) tmem_st32(tS + i * 32, sr[i]);
+      } else {
+        uint32_t pk[C::P_COLS / 32][32];
+        if (valid >= C::BC) softmax_p_bf16<C, false>(sr, pk, c2, negm2, valid, rs2);
+        else softmax_p_bf16<C, true>(sr, pk, c2, negm2, valid, rs2);
+#pragma unroll
+        for (int i = 0; i < C::P_COLS / 32; ++i) tmem_st32(tS + i * 32, pk[i]);
+      }
+      // correction of O_t: its last update (P V of step j-1) completed before S_t of step j did,
+      // and P V of step j is not issued before this warpgroup arrives below
       if (j > 0 && __any_sync(0xffffffffu, need)) {
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < C::D / 32; ++cc) {
           uint32_t orr[32];
@@ -341,54 +408,18 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           tmem_wait_ld();
           reg_fence(orr);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t v = f2_mul(f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2);
+            f2_unpack(v, orr[e], orr[e + 1]);
+          }
           tmem_st32(tO + cc * 32, orr);
         }
       }
-      // P = 2^(s*c - m_ref), row sum in fp32
-      const float neg_m = -m_ref;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
-      if (valid >= C::BC) {
-#pragma unroll
-        for (int i = 0; i < C::BC / 32; ++i)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float pv = ex2_approx(fmaf(__uint_as_float(sr[i][e]), c, neg_m));
-            rs[e & 3] += pv;
-            sr[i][e] = __float_as_uint(pv);
-          }
-      } else {  // ragged last tile: padded key columns get P = 0
-#pragma unroll
-        for (int i = 0; i < C::BC / 32; ++i)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float pv = (i * 32 + e < valid) ? ex2_approx(fmaf(__uint_as_float(sr[i][e]), c, neg_m)) : 0.f;
-            rs[e & 3] += pv;
-            sr[i][e] = __float_as_uint(pv);
-          }
-      }
-      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-      if constexpr (C::TF32) {  // round P to the nearest tf32 (the MMA would truncate)
-#pragma unroll
-        for (int i = 0; i < C::BC / 32; ++i) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(sr[i][e]) : "f"(__uint_as_float(sr[i][e])));
-          tmem_st32(tS + i * 32, sr[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < C::P_COLS / 32; ++i) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = i * 64 + 2 * e;  // two bf16 per 32-bit column, even element in the low half
-            pk[e] = pack_bf16x2(__uint_as_float(sr[col / 32][col % 32]),
-                                __uint_as_float(sr[(col + 1) / 32][(col + 1) % 32]));
-          }
-          tmem_st32(tS + i * 32, pk);
-        }
-      }
       tmem_wait_st();
+      float r0, r1, r2, r3;
+      f2_unpack_f(rs2[0], r0, r1);
+      f2_unpack_f(rs2[1], r2, r3);
+      l = l * alpha + ((r0 + r1) + (r2 + r3));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pf(t));
