@@ -43,9 +43,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     """Compile (if stale or forced) and return the path of libfa.so.
 
     FA_PTXAS_VERBOSE=1 in the environment adds ``-Xptxas -v`` and keeps its
-    register / spill report in _build/ptxas.log.
+    register / spill report in _build/ptxas.log.  FA_NVCC_EXTRA adds compiler
+    flags (e.g. tile-configuration definitions for tuning builds); a build
+    with different extra flags is always redone.
     """
-    if not force and not is_stale():
+    extra = os.environ.get("FA_NVCC_EXTRA", "").split()
+    stamp = os.path.join(OUT, "flags.txt")
+    prev = open(stamp).read() if os.path.exists(stamp) else ""
+    if not force and not is_stale() and prev == " ".join(extra):
         return LIB
     os.makedirs(OUT, exist_ok=True)
     nvcc = _nvcc()
@@ -54,6 +59,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     "--expt-relaxed-constexpr"]
     if ptxas_v:
         flags += ["-Xptxas", "-v"]
+    flags += extra
 
     def compile_one(src: str):
         obj = os.path.join(OUT, src.replace(".cu", ".o"))
@@ -79,6 +85,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc link failed")
     os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(" ".join(extra))
     return LIB
 
 

@@ -1,16 +1,46 @@
 // fa_fwd_bf16.cu -- bf16 instantiations of the fused forward kernel.
-//   d = 64 : Bc = 128, two 128-row query tiles per CTA, 4-stage K/V ring (160 KB shared)
-//   d = 128: Bc = 128, two 128-row query tiles per CTA, 2-stage K/V ring (192 KB shared)
+// Template arguments: head dim, key tile Bc, 128-row query tiles per CTA, K/V ring stages, CTAs per SM.
+//   d = 64 : Bc = 64, two query tiles per CTA, 4-stage K/V ring (96 KB shared), 2 CTAs/SM
+//            (four softmax warpgroups per SM: the d = 64 softmax is as costly as its MMAs)
+//   d = 128: Bc = 128, two query tiles per CTA, 2-stage K/V ring (192 KB shared), 1 CTA/SM
+// Compiler definitions FA_D64_{BC,NQT,STAGES,MINB} / FA_D128_{...} override the
+// tile configuration for tuning builds.
 #include <cuda_bf16.h>
 
 #include "fa_fwd_kernel.cuh"
 
+#ifndef FA_D64_BC
+#define FA_D64_BC 64
+#endif
+#ifndef FA_D64_NQT
+#define FA_D64_NQT 2
+#endif
+#ifndef FA_D64_STAGES
+#define FA_D64_STAGES 4
+#endif
+#ifndef FA_D64_MINB
+#define FA_D64_MINB 2
+#endif
+#ifndef FA_D128_BC
+#define FA_D128_BC 128
+#endif
+#ifndef FA_D128_NQT
+#define FA_D128_NQT 2
+#endif
+#ifndef FA_D128_STAGES
+#define FA_D128_STAGES 2
+#endif
+#ifndef FA_D128_MINB
+#define FA_D128_MINB 1
+#endif
+
 namespace fa {
 
-using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, 128, 2, 4>;
-using CfgBf16D128 = FwdCfg<__nv_bfloat16, 128, 128, 2, 2>;
+using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, FA_D64_BC, FA_D64_NQT, FA_D64_STAGES, FA_D64_MINB>;
+using CfgBf16D128 = FwdCfg<__nv_bfloat16, 128, FA_D128_BC, FA_D128_NQT, FA_D128_STAGES, FA_D128_MINB>;
 
 cudaError_t launch_fwd_bf16_d64(const FwdLaunch& a) { return launch_fwd<CfgBf16D64>(a); }
 cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a) { return launch_fwd<CfgBf16D128>(a); }
+int fwd_bc_bf16(int d) { return d == 64 ? CfgBf16D64::BC : CfgBf16D128::BC; }
 
 }  // namespace fa

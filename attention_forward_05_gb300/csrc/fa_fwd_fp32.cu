@@ -16,7 +16,7 @@ cudaError_t launch_fwd_fp32_d64(const FwdLaunch& a) { return launch_fwd<CfgF32D6
 cudaError_t launch_fwd_fp32_d128(const FwdLaunch& a) { return launch_fwd<CfgF32D128>(a); }
 
 FwdGeometry fwd_geometry(int dtype_is_bf16, int d) {
-  if (dtype_is_bf16) return FwdGeometry{64, 128, 128, 0};
+  if (dtype_is_bf16) return FwdGeometry{64, 128, fwd_bc_bf16(d), 0};
   return FwdGeometry{32, 128, d == 64 ? CfgF32D64::BC : CfgF32D128::BC, 1};
 }
 

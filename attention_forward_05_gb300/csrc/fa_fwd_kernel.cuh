@@ -37,13 +37,14 @@
 
 namespace fa {
 
-template <typename T, int D_, int BC_, int NQT_, int STAGES_>
+template <typename T, int D_, int BC_, int NQT_, int STAGES_, int MINB_ = 1>
 struct FwdCfg {
   using Elem = T;
   static constexpr int D = D_;
   static constexpr int BC = BC_;
   static constexpr int NQT = NQT_;
   static constexpr int STAGES = STAGES_;
+  static constexpr int MINB = MINB_;  // CTAs per SM the launch bounds ask for
   static constexpr int BR = 128;
   static constexpr int ESZ = static_cast<int>(sizeof(T));
   static constexpr bool TF32 = (ESZ == 4);
@@ -80,8 +81,8 @@ struct FwdCfg {
   static constexpr int MMA_WARP = 4 * NQT + 1;
   static_assert(D % CHUNK == 0, "head dim must be a whole number of 128-byte segments");
   static_assert(BC % 32 == 0 && BC >= 32 && BC <= 256, "key tile");
-  static_assert(TMEM_NEED <= 512, "tensor memory");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(TMEM_NEED <= 512 / MINB, "tensor memory");
+  static_assert(SMEM_BYTES * MINB <= 227 * 1024, "shared memory");
 };
 
 struct FwdParams {
@@ -125,10 +126,18 @@ __device__ __forceinline__ void softmax_p_bf16(const uint32_t (&sr)[C::BC / 32][
 #pragma unroll
   for (int qc = 0; qc < C::P_COLS; ++qc) {
     const int e0 = 2 * qc;
+#ifdef FA_SOFTMAX_SCALAR  // tuning build: scalar FFMA instead of the packed pair
+    float c_, nm_, d_;
+    f2_unpack_f(c2, c_, d_);
+    f2_unpack_f(negm2, nm_, d_);
+    const float x0 = fmaf(__uint_as_float(sr[e0 / 32][e0 % 32]), c_, nm_);
+    const float x1 = fmaf(__uint_as_float(sr[e0 / 32][e0 % 32 + 1]), c_, nm_);
+#else
     const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e0 / 32][e0 % 32]), __uint_as_float(sr[e0 / 32][e0 % 32 + 1])),
                               c2, negm2);
     float x0, x1;
     f2_unpack_f(x, x0, x1);
+#endif
     float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
     if (TAIL) {
       if (e0 >= valid) p0 = 0.f;
@@ -161,7 +170,7 @@ __device__ __forceinline__ void softmax_p_tf32(uint32_t (&sr)[C::BC / 32][32], u
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::NTHREADS, 1)
+__global__ void __launch_bounds__(C::NTHREADS, C::MINB)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -222,9 +231,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
   if (warp == C::LOAD_WARP) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int nk_issued[C::STAGES], nv_issued[C::STAGES];
-#pragma unroll
-      for (int s = 0; s < C::STAGES; ++s) nk_issued[s] = nv_issued[s] = 0;
+      int nk_done = 0, nv_done = 0;  // key tiles whose K (resp. V) copy was issued: tiles 0 .. n-1
       mbar_expect_tx(bar_q, C::NQT * C::Q_BYTES);
 #pragma unroll
       for (int t = 0; t < C::NQT; ++t)
@@ -242,8 +249,8 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sbase + C::OFF_K + s * C::KV_BYTES + c * C::KV_CH_BYTES, &tm_k, bar_kf(s),
                         c * C::CHUNK, j * C::BC, bh);
-          ++nk_issued[s];
         }
+        nk_done = j + 1;
         if (!mbar_wait(bar_ve(s), ph, abort_flag, p.err, W_VE)) break;
         mbar_expect_tx(bar_vf(s), C::KV_BYTES);
 #pragma unroll
@@ -255,14 +262,18 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             tma_load_3d(sbase + C::OFF_V + s * C::KV_BYTES + c * C::V_CH_BYTES, &tm_v, bar_vf(s), c * C::CHUNK,
                         j * C::BC, bh);
         }
-        ++nv_issued[s];
+        nv_done = j + 1;
       }
-      // Drain: every copy this thread issued must land before the CTA exits.
+      // Drain: every copy this thread issued must land before the CTA exits.  Stage s received
+      // the tiles j < n with j % STAGES == s; the last of them completes phase (count - 1).
       mbar_wait_drain(bar_q, 0, p.err, W_DRAIN_K);
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) {
-        if (nk_issued[s] > 0) mbar_wait_drain(bar_kf(s), (nk_issued[s] - 1) & 1, p.err, W_DRAIN_K);
-        if (nv_issued[s] > 0) mbar_wait_drain(bar_vf(s), (nv_issued[s] - 1) & 1, p.err, W_DRAIN_V);
+        int nks = (nk_done > s) ? (nk_done - 1 - s) / C::STAGES + 1 : 0;
+        if (p.fault == 1 && s == 0 && nk_done > 0) --nks;  // the skipped copy of tile 0
+        const int nvs = (nv_done > s) ? (nv_done - 1 - s) / C::STAGES + 1 : 0;
+        if (nks > 0) mbar_wait_drain(bar_kf(s), (nks - 1) & 1, p.err, W_DRAIN_K);
+        if (nvs > 0) mbar_wait_drain(bar_vf(s), (nvs - 1) & 1, p.err, W_DRAIN_V);
       }
     }
   } else if (warp == C::MMA_WARP) {

@@ -30,6 +30,7 @@ struct FwdGeometry {
 };
 
 FwdGeometry fwd_geometry(int dtype_is_bf16, int d);
+int fwd_bc_bf16(int d);  // key-tile rows of the bf16 instantiation for head dim d
 
 // fp32 prep pass: qr = tf32(q), kr = tf32(k) (round to nearest), and the key-major copy
 // vt[bh][c][j] = tf32(v[bh][j][c]) for j < Nk, 0 for Nk <= j < Nk_pad.

@@ -16,6 +16,7 @@ import sys
 import torch
 
 import attention_forward_05_gb300 as fa
+from attention_forward_05_gb300 import accounting
 from attention_forward_05_gb300.inputs import WORKLOADS, merge_order, workload_inputs
 
 
@@ -25,6 +26,7 @@ def main(argv=None) -> int:
     ap.add_argument("--launches", type=int, default=2)
     ap.add_argument("--B", type=int, default=0)
     ap.add_argument("--H", type=int, default=0)
+    ap.add_argument("--time", action="store_true", help="time the launches with CUDA events and print the rate")
     a = ap.parse_args(argv)
     w = WORKLOADS[a.workload]
     if a.B:
@@ -33,14 +35,31 @@ def main(argv=None) -> int:
         w = dataclasses.replace(w, H=a.H)
     dev = torch.device("cuda:0")
     q, k, v = workload_inputs(w, device=dev)
-    torch.cuda.synchronize()
-    for _ in range(1 + a.launches):
+    order = torch.as_tensor(merge_order(w.splits, w.order_seed), device=dev) if w.splits else None
+    o = torch.empty_like(q) if not w.splits else None
+    lse = torch.empty((w.B, w.H, w.Nq), device=dev) if not w.splits else None
+
+    def run():
         if w.splits:
-            order = torch.as_tensor(merge_order(w.splits, w.order_seed), device=dev)
             fa.fa_decode_splitkv_ex(q, k, v, w.splits, merge_order=order)
         else:
-            fa.fa_fwd(q, k, v, scale=w.scale)
+            fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse)
+
     torch.cuda.synchronize()
+    run()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(a.launches):
+        run()
+    end.record()
+    torch.cuda.synchronize()
+    if a.time and a.launches:
+        ms = start.elapsed_time(end) / a.launches
+        if w.splits:
+            rate = f"{accounting.decode_min_bytes(w.B, w.H, w.Nk, w.d) / ms / 1e6:.1f} GB/s"
+        else:
+            rate = f"{accounting.fwd_flops(w.B, w.H, w.Nq, w.Nk, w.d) / ms / 1e9:.1f} TFLOP/s"
+        print(f"time: {w.name} {ms * 1e3:.1f} us/launch {rate}")
     if fa.fa_check_device_error() != fa.FA_OK:
         print("device timeout", file=sys.stderr)
         return 1
