@@ -33,11 +33,18 @@
 #ifndef FA_D128_MINB
 #define FA_D128_MINB 1
 #endif
+#ifndef FA_D64_SPLIT
+#define FA_D64_SPLIT 1
+#endif
+#ifndef FA_D128_SPLIT
+#define FA_D128_SPLIT 1
+#endif
 
 namespace fa {
 
-using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, FA_D64_BC, FA_D64_NQT, FA_D64_STAGES, FA_D64_MINB>;
-using CfgBf16D128 = FwdCfg<__nv_bfloat16, 128, FA_D128_BC, FA_D128_NQT, FA_D128_STAGES, FA_D128_MINB>;
+using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, FA_D64_BC, FA_D64_NQT, FA_D64_STAGES, FA_D64_MINB, FA_D64_SPLIT>;
+using CfgBf16D128 =
+    FwdCfg<__nv_bfloat16, 128, FA_D128_BC, FA_D128_NQT, FA_D128_STAGES, FA_D128_MINB, FA_D128_SPLIT>;
 
 cudaError_t launch_fwd_bf16_d64(const FwdLaunch& a) { return launch_fwd<CfgBf16D64>(a); }
 cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a) { return launch_fwd<CfgBf16D128>(a); }

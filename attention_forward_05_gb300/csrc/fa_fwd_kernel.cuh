@@ -37,14 +37,15 @@
 
 namespace fa {
 
-template <typename T, int D_, int BC_, int NQT_, int STAGES_, int MINB_ = 1>
+template <typename T, int D_, int BC_, int NQT_, int STAGES_, int MINB_ = 1, int SPLIT_ = 1>
 struct FwdCfg {
   using Elem = T;
   static constexpr int D = D_;
   static constexpr int BC = BC_;
   static constexpr int NQT = NQT_;
   static constexpr int STAGES = STAGES_;
-  static constexpr int MINB = MINB_;  // CTAs per SM the launch bounds ask for
+  static constexpr int MINB = MINB_;    // CTAs per SM the launch bounds ask for
+  static constexpr int SPLIT = SPLIT_;  // softmax warpgroups per query tile, each owning BC/SPLIT key columns
   static constexpr int BR = 128;
   static constexpr int ESZ = static_cast<int>(sizeof(T));
   static constexpr bool TF32 = (ESZ == 4);
@@ -67,7 +68,10 @@ struct FwdCfg {
   // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT], drain
   static constexpr int NBAR = 1 + 4 * STAGES + 3 * NQT + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  // exchange of partial row maxima / sums between the SPLIT warpgroups of a tile: [2 slots][NQT][SPLIT][128]
+  static constexpr int OFF_XCHG = OFF_MISC + 16;
+  static constexpr int XCHG_BYTES = SPLIT > 1 ? 2 * NQT * SPLIT * 128 * 4 : 0;
+  static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_BYTES + 1024;  // + slack to align the base to 1024
   static constexpr int MMA_K = 32 / ESZ;                  // K of one tcgen05.mma (32 bytes)
   static constexpr int O_COL0 = NQT * BC;                 // TMEM: S_t at t*BC, O_t at O_COL0 + t*D
   static constexpr int TMEM_NEED = NQT * (BC + D);
@@ -75,12 +79,23 @@ struct FwdCfg {
                                    : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int P_COLS = BC * ESZ / 4;  // 32-bit TMEM columns of one P row
   static constexpr int P_COLS_PER_K = MMA_K * ESZ / 4;
-  static constexpr int NWARPS = 4 * NQT + 2;
+  static constexpr int COLS = BC / SPLIT;         // key columns of one softmax thread
+  static constexpr int PCOLS_W = P_COLS / SPLIT;  // P columns written by one softmax warpgroup
+  static constexpr int OCOLS = D / SPLIT;         // O columns rescaled and stored by one softmax warpgroup
+  static constexpr int NSMWG = NQT * SPLIT;       // softmax warpgroups
+  static constexpr int NWARPS = 4 * NSMWG + 2;
   static constexpr int NTHREADS = 32 * NWARPS;
-  static constexpr int LOAD_WARP = 4 * NQT;
-  static constexpr int MMA_WARP = 4 * NQT + 1;
+  static constexpr int LOAD_WARP = 4 * NSMWG;
+  static constexpr int MMA_WARP = 4 * NSMWG + 1;
+  // Registers per thread: each of the SM's 4 sub-partitions holds 16384 registers and
+  // ceil(warps per SM / 4) warps, in 8-register steps.
+  static constexpr int WARPS_PER_SUBPART = (NWARPS * MINB + 3) / 4;
+  static constexpr int MAXREG_RAW = (16384 / (WARPS_PER_SUBPART * 32)) / 8 * 8;
+  static constexpr int MAXREG = MAXREG_RAW > 248 ? 248 : MAXREG_RAW;
   static_assert(D % CHUNK == 0, "head dim must be a whole number of 128-byte segments");
   static_assert(BC % 32 == 0 && BC >= 32 && BC <= 256, "key tile");
+  static_assert(COLS % 32 == 0 && PCOLS_W % 32 == 0 && OCOLS % 32 == 0, "split into whole 32-column chunks");
+  static_assert(NQT <= 8, "one named barrier per tile");
   static_assert(TMEM_NEED <= 512 / MINB, "tensor memory");
   static_assert(SMEM_BYTES * MINB <= 227 * 1024, "shared memory");
 };
@@ -99,9 +114,9 @@ enum : int { W_Q = 1, W_KF, W_VF, W_KE, W_VE, W_SF, W_PF, W_OD, W_DRAIN_MMA, W_D
 
 // Row maximum (MAX) or minimum of the BC scores a thread holds: 4 independent
 // chains over groups of 8 elements, two new elements per 3-input max/min.
-template <class C, bool MAX>
-__device__ __forceinline__ float row_extreme(const uint32_t (&sr)[C::BC / 32][32]) {
-  static_assert(C::BC % 8 == 0, "groups of 8");
+template <int NCOL, bool MAX>
+__device__ __forceinline__ float row_extreme(const uint32_t (&sr)[NCOL / 32][32]) {
+  static_assert(NCOL % 8 == 0, "groups of 8");
   float a[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -109,7 +124,7 @@ __device__ __forceinline__ float row_extreme(const uint32_t (&sr)[C::BC / 32][32
     a[u] = MAX ? fmaxf(x, y) : fminf(x, y);
   }
 #pragma unroll
-  for (int g = 1; g < C::BC / 8; ++g)
+  for (int g = 1; g < NCOL / 8; ++g)
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int e = 8 * g + 2 * u;  // e and e + 1 lie in the same 32-column chunk
@@ -120,11 +135,11 @@ __device__ __forceinline__ float row_extreme(const uint32_t (&sr)[C::BC / 32][32
 }
 
 // bf16 P: for 32-bit column q, elements 2q (low half) and 2q+1 (high half) of the row.
-template <class C, bool TAIL>
-__device__ __forceinline__ void softmax_p_bf16(const uint32_t (&sr)[C::BC / 32][32], uint32_t (&pk)[C::P_COLS / 32][32],
+template <int NCOL, bool TAIL>
+__device__ __forceinline__ void softmax_p_bf16(const uint32_t (&sr)[NCOL / 32][32], uint32_t (&pk)[NCOL / 64][32],
                                                uint64_t c2, uint64_t negm2, int valid, uint64_t (&rs2)[2]) {
 #pragma unroll
-  for (int qc = 0; qc < C::P_COLS; ++qc) {
+  for (int qc = 0; qc < NCOL / 2; ++qc) {
     const int e0 = 2 * qc;
 #ifdef FA_SOFTMAX_SCALAR  // tuning build: scalar FFMA instead of the packed pair
     float c_, nm_, d_;
@@ -149,11 +164,11 @@ __device__ __forceinline__ void softmax_p_bf16(const uint32_t (&sr)[C::BC / 32][
 }
 
 // tf32 P: one element per 32-bit column, rounded to the nearest tf32 (the MMA would truncate).
-template <class C, bool TAIL>
-__device__ __forceinline__ void softmax_p_tf32(uint32_t (&sr)[C::BC / 32][32], uint64_t c2, uint64_t negm2, int valid,
+template <int NCOL, bool TAIL>
+__device__ __forceinline__ void softmax_p_tf32(uint32_t (&sr)[NCOL / 32][32], uint64_t c2, uint64_t negm2, int valid,
                                                uint64_t (&rs2)[2]) {
 #pragma unroll
-  for (int e0 = 0; e0 < C::BC; e0 += 2) {
+  for (int e0 = 0; e0 < NCOL; e0 += 2) {
     const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e0 / 32][e0 % 32]), __uint_as_float(sr[e0 / 32][e0 % 32 + 1])),
                               c2, negm2);
     float x0, x1;
@@ -170,7 +185,7 @@ __device__ __forceinline__ void softmax_p_tf32(uint32_t (&sr)[C::BC / 32][32], u
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::NTHREADS, C::MINB)
+__global__ void __maxnreg__(C::MAXREG)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -208,7 +223,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
     }
     for (int t = 0; t < C::NQT; ++t) {
       mbar_init(bar_sf(t), 1);
-      mbar_init(bar_pf(t), 4);  // one arrive per softmax warp
+      mbar_init(bar_pf(t), 4 * C::SPLIT);  // one arrive per softmax warp of the tile
       mbar_init(bar_od(t), 1);
     }
     mbar_init(bar_drain, 1);
@@ -352,40 +367,67 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int t = warp >> 2;
+    // Warpgroup g = warp / 4 owns query tile t = g / SPLIT and key columns
+    // [h * COLS, (h + 1) * COLS) of every key tile, h = g % SPLIT; thread = query row.
+    const int g = warp >> 2;
+    const int t = g / C::SPLIT;
+    const int h = g % C::SPLIT;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + t * C::BC;
-    const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::D;
+    const uint32_t tS = tmem + lane_base + t * C::BC + h * C::COLS;
+    const uint32_t tP = tmem + lane_base + t * C::BC + h * C::PCOLS_W;
+    const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::D + h * C::OCOLS;
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCHG);
+    auto xidx = [&](int slot, int hh) { return ((slot * C::NQT + t) * C::SPLIT + hh) * 128 + row; };
     const float c = p.c;
     float m_ref = -INFINITY;
     float l = 0.f;
     bool ok = true;
     const uint64_t c2 = f2_pack(c, c);
     for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[C::BC / 32][32];
+      bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
+      okw = __all_sync(0xffffffffu, okw);
+      uint32_t sr[C::COLS / 32][32];
+      const int valid = p.Nk - j * C::BC - h * C::COLS;  // valid key columns in this part (may be <= 0)
+      float m_part = -INFINITY;
+      {  // loaded even when the wait gave up (then the values are stale and unused): a conditional
+         // load would keep the row in local memory
+        tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < C::BC / 32; ++i) tmem_ld32(tS + i * 32, sr[i]);
-      tmem_wait_ld();
+        for (int i = 0; i < C::COLS / 32; ++i) tmem_ld32(tS + i * 32, sr[i]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < C::BC / 32; ++i) reg_fence(sr[i]);
-
-      const int valid = p.Nk - j * C::BC;  // >= 1
-      if (valid < C::BC) {                  // ragged last tile: repeat column 0 so max/min ignore the pad
-        const uint32_t s0 = sr[0][0];
+        for (int i = 0; i < C::COLS / 32; ++i) reg_fence(sr[i]);
+        if (valid > 0) {
+          if (valid < C::COLS) {  // ragged last tile: repeat column 0 so max/min ignore the pad
+            const uint32_t s0 = sr[0][0];
 #pragma unroll
-        for (int i = 0; i < C::BC / 32; ++i)
+            for (int i = 0; i < C::COLS / 32; ++i)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (i * 32 + e >= valid) sr[i][e] = s0;
+              for (int e = 0; e < 32; ++e)
+                if (i * 32 + e >= valid) sr[i][e] = s0;
+          }
+          // extreme of the raw scores (max for scale >= 0, min for scale < 0), times scale*log2(e)
+          m_part = (c >= 0.f ? row_extreme<C::COLS, true>(sr) : row_extreme<C::COLS, false>(sr)) * c;
+        }
       }
-      // row extreme of the raw scores (max for scale >= 0, min for scale < 0), 3-input max/min
-      const float m_tile = (c >= 0.f ? row_extreme<C, true>(sr) : row_extreme<C, false>(sr)) * c;
+      float m_tile = m_part;
+      if constexpr (C::SPLIT > 1) {
+        // Exchange the partial maxima (double-buffered by step parity) and agree on continuing:
+        // the barrier's AND-reduction gives every thread of the tile the same decision, so the
+        // warpgroups of a tile always meet the same number of times.
+        xch[xidx(j & 1, h)] = m_part;
+        tc_fence_before();
+        ok = bar_red_and(1 + t, 128 * C::SPLIT, okw);
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < C::SPLIT; ++hh)
+          if (hh != h) m_tile = fmaxf(m_tile, xch[xidx(j & 1, hh)]);
+      } else {
+        ok = okw;
+      }
+      if (!ok) break;
       const float m_new = fmaxf(m_ref, m_tile);
       const bool need = m_new > m_ref + p.tau;  // always true on the first tile (m_ref = -inf)
       float alpha = 1.f;
@@ -397,23 +439,23 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
       const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
       uint64_t rs2[2] = {0ull, 0ull};
       if constexpr (C::TF32) {
-        if (valid >= C::BC) softmax_p_tf32<C, false>(sr, c2, negm2, valid, rs2);
-        else softmax_p_tf32<C, true>(sr, c2, negm2, valid, rs2);
+        if (valid >= C::COLS) softmax_p_tf32<C::COLS, false>(sr, c2, negm2, valid, rs2);
+        else softmax_p_tf32<C::COLS, true>(sr, c2, negm2, valid, rs2);
 #pragma unroll
-        for (int i = 0; i < C::BC / 32; ++i) tmem_st32(tS + i * 32, sr[i]);
+        for (int i = 0; i < C::COLS / 32; ++i) tmem_st32(tP + i * 32, sr[i]);
       } else {
-        uint32_t pk[C::P_COLS / 32][32];
-        if (valid >= C::BC) softmax_p_bf16<C, false>(sr, pk, c2, negm2, valid, rs2);
-        else softmax_p_bf16<C, true>(sr, pk, c2, negm2, valid, rs2);
+        uint32_t pk[C::PCOLS_W / 32][32];
+        if (valid >= C::COLS) softmax_p_bf16<C::COLS, false>(sr, pk, c2, negm2, valid, rs2);
+        else softmax_p_bf16<C::COLS, true>(sr, pk, c2, negm2, valid, rs2);
 #pragma unroll
-        for (int i = 0; i < C::P_COLS / 32; ++i) tmem_st32(tS + i * 32, pk[i]);
+        for (int i = 0; i < C::PCOLS_W / 32; ++i) tmem_st32(tP + i * 32, pk[i]);
       }
       // correction of O_t: its last update (P V of step j-1) completed before S_t of step j did,
-      // and P V of step j is not issued before this warpgroup arrives below
+      // and P V of step j is not issued before every warpgroup of the tile arrives below
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int cc = 0; cc < C::D / 32; ++cc) {
+        for (int cc = 0; cc < C::OCOLS / 32; ++cc) {
           uint32_t orr[32];
           tmem_ld32(tO + cc * 32, orr);
           tmem_wait_ld();
@@ -436,18 +478,29 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
       if (lane == 0) mbar_arrive(bar_pf(t));
     }
     // ---------------------------------------------------------- epilogue: O / l, LSE
-    if (ok) {
-      ok = mbar_wait(bar_od(t), 0, abort_flag, p.err, W_OD);
-      ok = __all_sync(0xffffffffu, ok);
+    if (ok) {  // `ok` agrees across the warpgroups of the tile here
+      bool okw = mbar_wait(bar_od(t), 0, abort_flag, p.err, W_OD);
+      okw = __all_sync(0xffffffffu, okw);
+      if constexpr (C::SPLIT > 1) {  // total row sum from the partial sums (slot T & 1 is free)
+        xch[xidx(T & 1, h)] = l;
+        ok = bar_red_and(1 + t, 128 * C::SPLIT, okw);
+        float lt = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < C::SPLIT; ++hh) lt += xch[xidx(T & 1, hh)];
+        l = lt;
+      } else {
+        ok = okw;
+      }
     }
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const int qrow = q0 + t * C::BR + row;
       const bool in_range = qrow < p.Nq;
-      uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * C::ESZ);
+      uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * C::ESZ) +
+                      h * C::OCOLS * C::ESZ;
 #pragma unroll
-      for (int cc = 0; cc < C::D / 32; ++cc) {
+      for (int cc = 0; cc < C::OCOLS / 32; ++cc) {
         uint32_t orr[32];
         tmem_ld32(tO + cc * 32, orr);
         tmem_wait_ld();
@@ -478,7 +531,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB)
           }
         }
       }
-      if (p.lse != nullptr && in_range)
+      if (h == 0 && p.lse != nullptr && in_range)
         p.lse[static_cast<size_t>(bh) * p.Nq + qrow] = (m_ref + log2f(l)) * 0.6931471805599453f;
     }
   }
