@@ -55,6 +55,26 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks (the list itself when not distributed).
+
+    Timing rule: every rank times the same K steps, and the job's time is the
+    slowest rank's.
+    """
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_rate(units_per_rank: float, world: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: units every rank processed per step, over the slowest rank's time."""
+    return world * steps * units_per_rank / seconds
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -310,17 +330,14 @@ def run_gpu(args):
     dec_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     pre_ms = {n: [ev[i][1 + j].elapsed_time(ev[i][2 + j]) for i in range(K)] for j, n in enumerate(PREFILL)}
 
-    t = torch.tensor([total_ms, sum(dec_ms), sum(sum(x) for x in pre_ms.values())], dtype=torch.float64,
-                     device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, dec_tot, pre_tot = (float(x) for x in t.tolist())
+    total_ms, dec_tot, pre_tot = max_over_ranks(
+        [total_ms, sum(dec_ms), sum(sum(x) for x in pre_ms.values())], device=dev)
 
     pre_flops = {n: accounting.fwd_flops(w.B, w.H, w.Nq, w.Nk, w.d) for n, (w, *_r) in pre.items()}
     flops_step = sum(pre_flops.values())
-    value = world * K * flops_step / (pre_tot / 1e3) / 1e12
+    value = job_rate(flops_step, world, K, pre_tot / 1e3) / 1e12
     dec_bytes = accounting.decode_min_bytes(wd.B, wd.H, wd.Nk, wd.d)
-    dec_gbs = world * K * dec_bytes / (dec_tot / 1e3) / 1e9
+    dec_gbs = job_rate(dec_bytes, world, K, dec_tot / 1e3) / 1e9
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = e2e_dec = None
