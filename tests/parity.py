@@ -81,6 +81,7 @@ def check_fwd(q, k, v, o, lse, scale: float, rows=None, name: str = "") -> dict:
         if dt == "fp32":
             lse_tol = np.maximum(lse_tol, tf32_score_bound(qs, k, scale))
         assert (le <= lse_tol).all(), f"{name}: max|dLSE| {res['lse']:.3e} above its bound"
+    print(f"[parity] {name}: " + " ".join(f"{k}={v:.3e}" for k, v in res.items()))
     return res
 
 
@@ -125,4 +126,5 @@ def check_decode(q, k, v, o, lse, scale: float, splits: int, order=None, heads=N
         le = np.abs(lf.cpu().numpy().astype(np.float64) - ref_lse)
         res["lse"] = float(le.max())
         assert res["lse"] <= tol["lse"], f"{name}: max|dLSE| {res['lse']:.3e}"
+    print(f"[parity] {name}: " + " ".join(f"{k}={v:.3e}" for k, v in res.items()))
     return res
