@@ -293,76 +293,92 @@ __global__ void __maxnreg__(C::MAXREG)
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop, so descriptors and addresses are warp-uniform (uniform
+    // registers); one elected lane issues each tcgen05 instruction.  Waits are taken by all lanes
+    // and agreed with __all_sync.
+    {
+      auto wait_all = [&](uint32_t bar, uint32_t parity, int where) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where));
+      };
       constexpr uint32_t idesc_qk = make_idesc(C::FMT, C::BR, C::BC, 0, 0);
       constexpr uint32_t idesc_pv = make_idesc(C::FMT, C::BR, C::D, 0, C::V_KMAJOR ? 0 : 1);
+      // Shared-memory descriptors are built once; each MMA only adds a compile-time offset to the
+      // address field (bytes >> 4, bits 0-13: every address here is below 256 KB, so no carry).
+      // Rebuilding them per instruction made the issuing thread, not the tensor core, the bottleneck.
+      const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dv0 = C::V_KMAJOR ? sdesc_sw128(sbase + C::OFF_V, 16, 1024)
+                                       : sdesc_sw128(sbase + C::OFF_V, C::V_CH_BYTES, 1024);
       auto issue_qk = [&](int t, int s) {
         const uint32_t d_tmem = tmem + t * C::BC;
+        const uint64_t qa = dq0 + static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
+        const uint64_t kb = dk0 + static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-          const int e = kk * C::MMA_K;
-          const uint32_t off = (e % C::CHUNK) * C::ESZ;  // byte offset inside the 128-byte segment
-          const uint32_t qa = sbase + C::OFF_Q + t * C::Q_BYTES + (e / C::CHUNK) * C::Q_CH_BYTES + off;
-          const uint32_t kb = sbase + C::OFF_K + s * C::KV_BYTES + (e / C::CHUNK) * C::KV_CH_BYTES + off;
-          mma_ss<C::TF32>(d_tmem, sdesc_sw128(qa, 16, 1024), sdesc_sw128(kb, 16, 1024), idesc_qk, kk > 0);
+          const int e = kk * C::MMA_K;  // element offset along d: 128-byte segment, then 32-byte step inside it
+          const uint32_t oq = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * C::ESZ) >> 4;
+          const uint32_t ok_ = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * C::ESZ) >> 4;
+          if (elect_one()) mma_ss<C::TF32>(d_tmem, qa + oq, kb + ok_, idesc_qk, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
         const uint32_t d_tmem = tmem + C::O_COL0 + t * C::D;
         const uint32_t a_tmem = tmem + t * C::BC;
+        const uint64_t vb = dv0 + static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
-          uint64_t vdesc;
+          uint32_t ov;
           if constexpr (C::V_KMAJOR) {  // [D rows][Bc keys]: step along keys inside 128-byte segments
             const int e = kk * C::MMA_K;
-            vdesc = sdesc_sw128(sbase + C::OFF_V + s * C::KV_BYTES + (e / C::CHUNK) * C::V_CH_BYTES +
-                                    (e % C::CHUNK) * C::ESZ,
-                                16, 1024);
+            ov = ((e / C::CHUNK) * C::V_CH_BYTES + (e % C::CHUNK) * C::ESZ) >> 4;
           } else {  // [Bc keys][D]: MN-major, 8-key groups 1024 B apart, 64-column segments LBO apart
-            vdesc = sdesc_sw128(sbase + C::OFF_V + s * C::KV_BYTES + kk * C::MMA_K * 128, C::V_CH_BYTES, 1024);
+            ov = (kk * C::MMA_K * 128) >> 4;
           }
-          mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_K, vdesc, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          if (elect_one())
+            mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_K, vb + ov, idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, W_Q) && mbar_wait(bar_kf(0), 0, abort_flag, p.err, W_KF);
+      auto commit = [&](uint32_t bar) {
+        if (elect_one()) mma_commit(bar);
+        __syncwarp();
+      };
+      bool ok = wait_all(bar_q, 0, W_Q) && wait_all(bar_kf(0), 0, W_KF);
       if (ok) {
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < C::NQT; ++t) {
           issue_qk(t, 0);
-          mma_commit(bar_sf(t));
+          commit(bar_sf(t));
         }
-        mma_commit(bar_ke(0));
+        commit(bar_ke(0));
       }
       for (int j = 0; ok && j < T; ++j) {
         const int s = j % C::STAGES;
         const int j1 = j + 1;
         const int s1 = j1 % C::STAGES;
-        ok = mbar_wait(bar_vf(s), (j / C::STAGES) & 1, abort_flag, p.err, W_VF);
+        // V_j and K_{j+1} are normally resident long before P_t(j) is ready: wait for them first so
+        // the chain P ready -> P V -> next Q K^T holds nothing but MMA issue.
+        ok = wait_all(bar_vf(s), (j / C::STAGES) & 1, W_VF);
+        if (ok && j1 < T) ok = wait_all(bar_kf(s1), (j1 / C::STAGES) & 1, W_KF);
         if (!ok) break;
 #pragma unroll
         for (int t = 0; t < C::NQT; ++t) {
-          ok = mbar_wait(bar_pf(t), j & 1, abort_flag, p.err, W_PF);
+          ok = wait_all(bar_pf(t), j & 1, W_PF);
           if (!ok) break;
           tc_fence_after();
           issue_pv(t, s, j > 0);
-          if (t == C::NQT - 1) mma_commit(bar_ve(s));
+          if (t == C::NQT - 1) commit(bar_ve(s));
           if (j1 < T) {
-            if (t == 0) {
-              ok = mbar_wait(bar_kf(s1), (j1 / C::STAGES) & 1, abort_flag, p.err, W_KF);
-              if (!ok) break;
-              tc_fence_after();
-            }
             issue_qk(t, s1);
-            mma_commit(bar_sf(t));
-            if (t == C::NQT - 1) mma_commit(bar_ke(s1));
+            commit(bar_sf(t));
+            if (t == C::NQT - 1) commit(bar_ke(s1));
           } else {
-            mma_commit(bar_od(t));
+            commit(bar_od(t));
           }
         }
       }
       // Drain: all MMAs issued above complete before tensor memory is freed.
-      mma_commit(bar_drain);
+      commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, p.err, W_DRAIN_MMA);
     }
   } else {
@@ -469,13 +485,13 @@ __global__ void __maxnreg__(C::MAXREG)
         }
       }
       tmem_wait_st();
-      float r0, r1, r2, r3;
-      f2_unpack_f(rs2[0], r0, r1);
-      f2_unpack_f(rs2[1], r2, r3);
-      l = l * alpha + ((r0 + r1) + (r2 + r3));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pf(t));
+      float r0, r1, r2, r3;  // the row sum is not needed by the MMA: update it after the signal
+      f2_unpack_f(rs2[0], r0, r1);
+      f2_unpack_f(rs2[1], r2, r3);
+      l = l * alpha + ((r0 + r1) + (r2 + r3));
     }
     // ---------------------------------------------------------- epilogue: O / l, LSE
     if (ok) {  // `ok` agrees across the warpgroups of the tile here
