@@ -7,7 +7,9 @@ library's CUDA kernels; there is no fallback.  If the library is missing or
 fails to load, importing the binding's entry points raises.
 
 Entry points (same names as the C ABI):
-  fa_fwd(q, k, v, scale=None, o=None, lse=None, with_lse=True) -> (o, lse)
+  fa_fwd(q, k, v, scale=None, o=None, lse=None, with_lse=True, kv_splits=0, causal=False, workspace=None)
+      -> (o, lse)      (calls fa_fwd_ex; k/v may have fewer heads than q)
+  fa_fwd_workspace_bytes(B, H, Hkv, Nq, Nk, d, dtype, causal, kv_splits)
   fa_decode_splitkv(q, k, v, splits, o=None) -> o
   fa_decode_splitkv_ex(q, k, v, splits, scale=None, workspace=None, merge_order=None, with_lse=False)
   fa_decode_workspace_bytes(B, H, d, splits)
@@ -55,6 +57,10 @@ def lib() -> ctypes.CDLL:
             vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
             L.fa_fwd.restype = i
+            L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp, sz, vp]
+            L.fa_fwd_ex.restype = i
+            L.fa_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
+            L.fa_fwd_workspace_bytes.restype = sz
             L.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
             L.fa_decode_splitkv.restype = i
             L.fa_decode_splitkv_ex.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp, vp, vp]
@@ -106,16 +112,23 @@ def _need_cuda_contig(name: str, t: torch.Tensor) -> None:
 
 def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
            o: torch.Tensor | None = None, lse: torch.Tensor | None = None, with_lse: bool = True,
-           stream=None):
-    """Exact attention softmax(q k^T * scale) v over [B, H, N, d] tensors; returns (o, lse or None)."""
+           stream=None, kv_splits: int = 0, causal: bool = False, workspace: torch.Tensor | None = None):
+    """Exact attention softmax(q k^T * scale) v; returns (o, lse or None).
+
+    q [B, H, Nq, d]; k, v [B, Hkv, Nk, d] with H a multiple of Hkv (grouped-query
+    attention when Hkv < H).  kv_splits: 0 automatic, 1 none, n > 1 split keys.
+    Calls fa_fwd_ex.
+    """
     for n, t in (("q", q), ("k", k), ("v", v)):
         _need_cuda_contig(n, t)
-    if q.dim() != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
-        raise ValueError("q [B,H,Nq,d], k/v [B,H,Nk,d] expected")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d], k/v [B,Hkv,Nk,d] expected")
+    if q.shape[1] % k.shape[1] != 0:
+        raise ValueError("query heads must be a multiple of key/value heads")
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share a dtype")
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
+    Hkv, Nk = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if o is None:
@@ -129,11 +142,22 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | Non
         _need_cuda_contig("lse", lse)
         if lse.shape != (B, H, Nq) or lse.dtype != torch.float32:
             raise ValueError("lse must be fp32 [B,H,Nq]")
-    st = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                      lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, float(scale),
-                      _dtype_code(q), _stream_handle(stream))
-    _check(st, "fa_fwd")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need_cuda_contig("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib().fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, B, H, Hkv, Nq, Nk, d, float(scale),
+                         _dtype_code(q), int(bool(causal)), int(kv_splits), ws_ptr, ws_bytes,
+                         _stream_handle(stream))
+    _check(st, "fa_fwd_ex")
     return o, lse
+
+
+def fa_fwd_workspace_bytes(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int, dtype=torch.bfloat16,
+                           causal: bool = False, kv_splits: int = 0) -> int:
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_FP32
+    return int(lib().fa_fwd_workspace_bytes(B, H, Hkv, Nq, Nk, d, code, int(bool(causal)), int(kv_splits)))
 
 
 def _decode_shapes(q, k, v):

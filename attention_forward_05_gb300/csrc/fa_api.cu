@@ -21,6 +21,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
 int g_cc_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+int g_sms[kMaxDevices] = {};    // multiprocessor count
 std::atomic<int> g_fault{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -34,7 +35,7 @@ int cuda_fail(cudaError_t e) {
 }
 
 // Per-device setup: checks the device is sm_103 and fetches the error word's address.
-int device_setup(int* dev_out, int** err_out) {
+int device_setup(int* dev_out, int** err_out, int* sms_out = nullptr) {
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return cuda_fail(ce);
@@ -46,6 +47,8 @@ int device_setup(int* dev_out, int** err_out) {
         (ce = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(ce);
     g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    if ((ce = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(ce);
   }
   if (g_cc_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
   if (g_err_ptr[dev] == nullptr) {
@@ -63,6 +66,7 @@ int device_setup(int* dev_out, int** err_out) {
   }
   *dev_out = dev;
   *err_out = g_err_ptr[dev];
+  if (sms_out) *sms_out = g_sms[dev];
   return FA_OK;
 }
 
@@ -110,52 +114,142 @@ int fa_debug_set_fault(int mode) {
   return FA_OK;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
-           float scale, int dtype, fa_stream_t stream) {
-  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
-  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Work split and workspace layout of one forward call.
+struct FwdPlan {
+  int n_split = 1, kv_per_split = 0, nk_pad = 0;
+  size_t off_qr = 0, off_kr = 0, off_vt = 0, off_wo = 0, off_wml = 0, total = 0;
+};
+
+// Validates the forward arguments that do not involve pointers.  sms = 0 means "device unknown"
+// (only allowed when kv_splits != 0).
+int plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype, int causal, int kv_splits, int sms,
+             FwdPlan* pl) {
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (causal != 0) return FA_ERR_UNSUPPORTED;
+  if (kv_splits < 0) return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
   if (BH * static_cast<long long>(Nq > Nk ? Nq : Nk) * d > kMaxElems) return FA_ERR_INVALID_ARG;
-  const bool bf16 = (dtype == FA_BF16);
+  const bool bf16 = dtype == FA_BF16;
+  const fa::FwdGeometry geo = fa::fwd_geometry(bf16 ? 1 : 0, d);
+  const long long tiles = (Nk + geo.kv_rows - 1) / geo.kv_rows;
+  long long n = kv_splits;
+  if (n == 0) {  // automatic: split the keys only when the query tiles cannot fill the GPU
+    if (sms <= 0) return FA_ERR_INVALID_ARG;
+    const long long ctas = ((Nq + geo.rows_per_cta - 1) / geo.rows_per_cta) * BH;
+    const long long slots = static_cast<long long>(sms) * geo.ctas_per_sm;
+    n = 1;
+    if (2 * ctas < slots) {
+      n = (slots + ctas - 1) / ctas;
+      const long long most = tiles / 2 > 1 ? tiles / 2 : 1;  // keep >= 2 key tiles per split
+      if (n > most) n = most;
+      if (n > 64) n = 64;
+    }
+  }
+  if (n > tiles) return FA_ERR_INVALID_ARG;
+  const long long per = ((tiles + n - 1) / n) * geo.kv_rows;
+  pl->kv_per_split = static_cast<int>(per);
+  pl->n_split = static_cast<int>((Nk + per - 1) / per);  // every split owns at least one key
+  size_t off = 0;
+  if (geo.v_kmajor) {
+    pl->nk_pad = (Nk + 3) & ~3;
+    const long long BHkv = static_cast<long long>(B) * Hkv;
+    pl->off_qr = off;
+    off += round256(static_cast<size_t>(BH) * Nq * d * sizeof(float));
+    pl->off_kr = off;
+    off += round256(static_cast<size_t>(BHkv) * Nk * d * sizeof(float));
+    pl->off_vt = off;
+    off += round256(static_cast<size_t>(BHkv) * d * pl->nk_pad * sizeof(float));
+  }
+  if (pl->n_split > 1) {
+    pl->off_wo = off;
+    off += round256(static_cast<size_t>(pl->n_split) * BH * Nq * d * sizeof(float));
+    pl->off_wml = off;
+    off += round256(static_cast<size_t>(pl->n_split) * BH * Nq * 2 * sizeof(float));
+  }
+  pl->total = off;
+  return FA_OK;
+}
 
-  int dev = 0;
+}  // namespace
+
+extern "C" {
+
+size_t fa_fwd_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype, int causal, int kv_splits) {
+  int sms = 0;
+  if (kv_splits == 0) {
+    int dev = 0;
+    int* err = nullptr;
+    if (device_setup(&dev, &err, &sms) != FA_OK) return 0;
+  }
+  FwdPlan pl;
+  if (plan_fwd(B, H, Hkv, Nq, Nk, d, dtype, causal, kv_splits, sms, &pl) != FA_OK) return 0;
+  return pl.total;
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
+              int Nk, int d, float scale, int dtype, int causal, int kv_splits, void* workspace,
+              size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
+  if (workspace && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  FwdPlan pl;
+  int rc = plan_fwd(B, H, Hkv, Nq, Nk, d, dtype, causal, kv_splits == 0 ? 1 : kv_splits, 0, &pl);
+  if (rc != FA_OK) return rc;  // argument errors are reported before touching the device
+
+  int dev = 0, sms = 0;
   int* err = nullptr;
-  int rc = device_setup(&dev, &err);
+  rc = device_setup(&dev, &err, &sms);
   if (rc != FA_OK) return rc;
+  if (kv_splits == 0 && (rc = plan_fwd(B, H, Hkv, Nq, Nk, d, dtype, causal, 0, sms, &pl)) != FA_OK) return rc;
+  if (workspace && workspace_bytes < pl.total) return FA_ERR_INVALID_ARG;
 
+  const bool bf16 = (dtype == FA_BF16);
+  const int BH = B * H, BHkv = B * Hkv;
   const fa::FwdGeometry geo = fa::fwd_geometry(bf16 ? 1 : 0, d);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  CUtensorMap tq, tk, tv;
-  void* ws = nullptr;  // fp32 path only: tf32-rounded Q and K, key-major tf32 V^T (stream-ordered)
-  if (geo.v_kmajor) {
-    const int nk_pad = (Nk + 3) & ~3;  // row stride of V^T must be a multiple of 16 bytes
-    const size_t qb = (static_cast<size_t>(BH) * Nq * d * sizeof(float) + 255) & ~static_cast<size_t>(255);
-    const size_t kb = (static_cast<size_t>(BH) * Nk * d * sizeof(float) + 255) & ~static_cast<size_t>(255);
-    const size_t vb = static_cast<size_t>(BH) * d * nk_pad * sizeof(float);
-    cudaError_t ea = cudaMallocAsync(&ws, qb + kb + vb, st);
+  char* ws = static_cast<char*>(workspace);
+  bool own_ws = false;
+  if (ws == nullptr && pl.total > 0) {
+    void* wp = nullptr;
+    cudaError_t ea = cudaMallocAsync(&wp, pl.total, st);
     if (ea != cudaSuccess) return cuda_fail(ea);
-    float* qr = static_cast<float*>(ws);
-    float* kr = reinterpret_cast<float*>(static_cast<char*>(ws) + qb);
-    float* vt = reinterpret_cast<float*>(static_cast<char*>(ws) + qb + kb);
-    ea = fa::launch_prep_fp32(static_cast<const float*>(q), static_cast<const float*>(k),
-                              static_cast<const float*>(v), qr, kr, vt, static_cast<int>(BH), Nq, Nk, nk_pad, d, st);
-    if (ea != cudaSuccess ||
-        encode_map(&tq, qr, false, static_cast<int>(BH), Nq, d, geo.box_cols, geo.q_rows) != FA_OK ||
-        encode_map(&tk, kr, false, static_cast<int>(BH), Nk, d, geo.box_cols, geo.kv_rows) != FA_OK ||
-        encode_map(&tv, vt, false, static_cast<int>(BH), d, nk_pad, 32, d) != FA_OK) {
-      cudaFreeAsync(ws, st);
-      return ea != cudaSuccess ? cuda_fail(ea) : FA_ERR_CUDA;
-    }
-  } else if (encode_map(&tq, q, bf16, static_cast<int>(BH), Nq, d, geo.box_cols, geo.q_rows) != FA_OK ||
-             encode_map(&tk, k, bf16, static_cast<int>(BH), Nk, d, geo.box_cols, geo.kv_rows) != FA_OK ||
-             encode_map(&tv, v, bf16, static_cast<int>(BH), Nk, d, geo.box_cols, geo.kv_rows) != FA_OK) {
-    return FA_ERR_CUDA;
+    ws = static_cast<char*>(wp);
+    own_ws = true;
+  }
+  auto fail = [&](cudaError_t e) {
+    if (own_ws) cudaFreeAsync(ws, st);
+    return e != cudaSuccess ? cuda_fail(e) : FA_ERR_CUDA;
+  };
+
+  CUtensorMap tq, tk, tv;
+  if (geo.v_kmajor) {  // fp32: tf32-rounded Q and K, key-major tf32 V^T (tf32 MMA operands are K-major)
+    float* qr = reinterpret_cast<float*>(ws + pl.off_qr);
+    float* kr = reinterpret_cast<float*>(ws + pl.off_kr);
+    float* vt = reinterpret_cast<float*>(ws + pl.off_vt);
+    cudaError_t ea = fa::launch_prep_fp32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                          static_cast<const float*>(v), qr, kr, vt, BH, BHkv, Nq, Nk, pl.nk_pad, d,
+                                          st);
+    if (ea != cudaSuccess) return fail(ea);
+    if (encode_map(&tq, qr, false, BH, Nq, d, geo.box_cols, geo.q_rows) != FA_OK ||
+        encode_map(&tk, kr, false, BHkv, Nk, d, geo.box_cols, geo.kv_rows) != FA_OK ||
+        encode_map(&tv, vt, false, BHkv, d, pl.nk_pad, 32, d) != FA_OK)
+      return fail(cudaSuccess);
+  } else if (encode_map(&tq, q, bf16, BH, Nq, d, geo.box_cols, geo.q_rows) != FA_OK ||
+             encode_map(&tk, k, bf16, BHkv, Nk, d, geo.box_cols, geo.kv_rows) != FA_OK ||
+             encode_map(&tv, v, bf16, BHkv, Nk, d, geo.box_cols, geo.kv_rows) != FA_OK) {
+    return fail(cudaSuccess);
   }
 
   fa::FwdLaunch a;
@@ -165,9 +259,15 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   a.o = o;
   a.lse = lse;
   a.err = err;
-  a.BH = static_cast<int>(BH);
+  a.BH = BH;
   a.Nq = Nq;
   a.Nk = Nk;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.kv_per_split = pl.kv_per_split;
+  a.n_split = pl.n_split;
+  a.ws_o = pl.n_split > 1 ? reinterpret_cast<float*>(ws + pl.off_wo) : nullptr;
+  a.ws_ml = pl.n_split > 1 ? reinterpret_cast<float*>(ws + pl.off_wml) : nullptr;
   a.c = scale * 1.4426950408889634f;
   a.tau = 8.0f;
   a.fault = g_fault.exchange(0);
@@ -177,11 +277,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     e = (d == 64) ? fa::launch_fwd_bf16_d64(a) : fa::launch_fwd_bf16_d128(a);
   else
     e = (d == 64) ? fa::launch_fwd_fp32_d64(a) : fa::launch_fwd_fp32_d128(a);
-  if (ws != nullptr) {
+  if (e == cudaSuccess && pl.n_split > 1)
+    e = fa::launch_fwd_merge(a.ws_o, a.ws_ml, o, lse, static_cast<long long>(BH) * Nq, d, pl.n_split, bf16 ? 1 : 0,
+                             st);
+  if (own_ws) {
     cudaError_t e2 = cudaFreeAsync(ws, st);
     if (e == cudaSuccess) e = e2;
   }
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
+           float scale, int dtype, fa_stream_t stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, H, H, Nq, Nk, d, scale, dtype, 0, 0, nullptr, 0, stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int d, int splits) {

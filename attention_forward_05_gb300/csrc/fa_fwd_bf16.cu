@@ -48,6 +48,10 @@ using CfgBf16D128 =
 
 cudaError_t launch_fwd_bf16_d64(const FwdLaunch& a) { return launch_fwd<CfgBf16D64>(a); }
 cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a) { return launch_fwd<CfgBf16D128>(a); }
-int fwd_bc_bf16(int d) { return d == 64 ? CfgBf16D64::BC : CfgBf16D128::BC; }
+FwdGeometry fwd_geometry_bf16(int d) {
+  if (d == 64)
+    return FwdGeometry{64, 128, CfgBf16D64::BC, 0, CfgBf16D64::BR * CfgBf16D64::NQT, CfgBf16D64::MINB};
+  return FwdGeometry{64, 128, CfgBf16D128::BC, 0, CfgBf16D128::BR * CfgBf16D128::NQT, CfgBf16D128::MINB};
+}
 
 }  // namespace fa

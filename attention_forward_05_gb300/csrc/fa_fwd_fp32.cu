@@ -16,8 +16,9 @@ cudaError_t launch_fwd_fp32_d64(const FwdLaunch& a) { return launch_fwd<CfgF32D6
 cudaError_t launch_fwd_fp32_d128(const FwdLaunch& a) { return launch_fwd<CfgF32D128>(a); }
 
 FwdGeometry fwd_geometry(int dtype_is_bf16, int d) {
-  if (dtype_is_bf16) return FwdGeometry{64, 128, fwd_bc_bf16(d), 0};
-  return FwdGeometry{32, 128, d == 64 ? CfgF32D64::BC : CfgF32D128::BC, 1};
+  if (dtype_is_bf16) return fwd_geometry_bf16(d);
+  if (d == 64) return FwdGeometry{32, 128, CfgF32D64::BC, 1, CfgF32D64::BR * CfgF32D64::NQT, CfgF32D64::MINB};
+  return FwdGeometry{32, 128, CfgF32D128::BC, 1, CfgF32D128::BR * CfgF32D128::NQT, CfgF32D128::MINB};
 }
 
 __device__ __forceinline__ float round_tf32(float x) {
@@ -62,15 +63,15 @@ __global__ void __launch_bounds__(256) round_tf32_kernel(const float4* __restric
 }
 
 cudaError_t launch_prep_fp32(const float* q, const float* k, const float* v, float* qr, float* kr, float* vt,
-                             int BH, int Nq, int Nk, int Nk_pad, int d, cudaStream_t stream) {
+                             int BH, int BHkv, int Nq, int Nk, int Nk_pad, int d, cudaStream_t stream) {
   const int n_kb = (Nk_pad + 31) / 32;
-  const long long gx = static_cast<long long>(n_kb) * BH;
+  const long long gx = static_cast<long long>(n_kb) * BHkv;
   if (gx <= 0 || gx > 0x7FFFFFFFLL || d % 32 != 0) return cudaErrorInvalidValue;
   transpose_v_kernel<<<dim3(static_cast<unsigned>(gx), d / 32), dim3(32, 8), 0, stream>>>(v, vt, Nk, Nk_pad, d,
                                                                                          n_kb);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t nq4 = static_cast<size_t>(BH) * Nq * d / 4, nk4 = static_cast<size_t>(BH) * Nk * d / 4;
+  const size_t nq4 = static_cast<size_t>(BH) * Nq * d / 4, nk4 = static_cast<size_t>(BHkv) * Nk * d / 4;
   const unsigned gq = static_cast<unsigned>(nq4 / 256 + 1 < 4096 ? nq4 / 256 + 1 : 4096);
   const unsigned gk = static_cast<unsigned>(nk4 / 256 + 1 < 4096 ? nk4 / 256 + 1 : 4096);
   round_tf32_kernel<<<gq, 256, 0, stream>>>(reinterpret_cast<const float4*>(q), reinterpret_cast<float4*>(qr), nq4);

@@ -105,6 +105,11 @@ struct FwdParams {
   float* lse;
   int* err;
   int Nq, Nk, n_qblk;
+  int BH, H, Hkv;       // query heads per batch H; key/value heads Hkv (H % Hkv == 0)
+  int kv_per_split;     // keys per split (a multiple of Bc); the CTA covers [split*kv_per_split, ...)
+  int n_split;          // 1: write O and LSE; > 1: write unnormalised partial states for the merge
+  float* ws_o;          // [n_split][BH][Nq][D] fp32 unnormalised O (split mode)
+  float* ws_ml;         // [n_split][BH][Nq][2] fp32 (m in log2 units, l) (split mode)
   float c, tau;
   int fault;
 };
@@ -195,10 +200,15 @@ __global__ void __maxnreg__(C::MAXREG)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // blockIdx.x = (split * BH + bh) * n_qblk + qb: CTAs sharing a head and key range are adjacent
   const int qb = blockIdx.x % p.n_qblk;
-  const int bh = blockIdx.x / p.n_qblk;
+  const int bh = (blockIdx.x / p.n_qblk) % p.BH;
+  const int split = blockIdx.x / (p.n_qblk * p.BH);
+  const int kvh = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);  // key/value head of this query head
   const int q0 = qb * C::BR * C::NQT;
-  const int T = (p.Nk + C::BC - 1) / C::BC;
+  const int k_begin = split * p.kv_per_split;
+  const int k_end = min(p.Nk, k_begin + p.kv_per_split);  // the host makes every split non-empty
+  const int T = (k_end - k_begin + C::BC - 1) / C::BC;
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_q = bar0;
@@ -263,7 +273,7 @@ __global__ void __maxnreg__(C::MAXREG)
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sbase + C::OFF_K + s * C::KV_BYTES + c * C::KV_CH_BYTES, &tm_k, bar_kf(s),
-                        c * C::CHUNK, j * C::BC, bh);
+                        c * C::CHUNK, k_begin + j * C::BC, kvh);
         }
         nk_done = j + 1;
         if (!mbar_wait(bar_ve(s), ph, abort_flag, p.err, W_VE)) break;
@@ -272,10 +282,10 @@ __global__ void __maxnreg__(C::MAXREG)
         for (int c = 0; c < C::NCH_V; ++c) {
           if constexpr (C::V_KMAJOR)
             tma_load_3d(sbase + C::OFF_V + s * C::KV_BYTES + c * C::V_CH_BYTES, &tm_v, bar_vf(s),
-                        j * C::BC + c * C::CHUNK, 0, bh);
+                        k_begin + j * C::BC + c * C::CHUNK, 0, kvh);
           else
             tma_load_3d(sbase + C::OFF_V + s * C::KV_BYTES + c * C::V_CH_BYTES, &tm_v, bar_vf(s), c * C::CHUNK,
-                        j * C::BC, bh);
+                        k_begin + j * C::BC, kvh);
         }
         nv_done = j + 1;
       }
@@ -405,7 +415,7 @@ __global__ void __maxnreg__(C::MAXREG)
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
       okw = __all_sync(0xffffffffu, okw);
       uint32_t sr[C::COLS / 32][32];
-      const int valid = p.Nk - j * C::BC - h * C::COLS;  // valid key columns in this part (may be <= 0)
+      const int valid = k_end - k_begin - j * C::BC - h * C::COLS;  // valid key columns here (may be <= 0)
       float m_part = -INFINITY;
       {  // loaded even when the wait gave up (then the values are stale and unused): a conditional
          // load would keep the row in local memory
@@ -508,7 +518,26 @@ __global__ void __maxnreg__(C::MAXREG)
         ok = okw;
       }
     }
-    if (ok) {
+    if (ok && p.n_split > 1) {  // partial state (m, l, unnormalised O) of this key range, for the merge
+      tc_fence_after();
+      const int qrow = q0 + t * C::BR + row;
+      const bool in_range = qrow < p.Nq;
+      const size_t srow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + qrow;
+      float* wrow = p.ws_o + srow * C::D + h * C::OCOLS;
+#pragma unroll
+      for (int cc = 0; cc < C::OCOLS / 32; ++cc) {
+        uint32_t orr[32];
+        tmem_ld32(tO + cc * 32, orr);
+        tmem_wait_ld();
+        reg_fence(orr);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(wrow + cc * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) dst[v4] = make_uint4(orr[4 * v4], orr[4 * v4 + 1], orr[4 * v4 + 2], orr[4 * v4 + 3]);
+        }
+      }
+      if (h == 0 && in_range) reinterpret_cast<float2*>(p.ws_ml)[srow] = make_float2(m_ref, l);
+    } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const int qrow = q0 + t * C::BR + row;
@@ -574,10 +603,20 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   p.Nq = a.Nq;
   p.Nk = a.Nk;
   p.n_qblk = (a.Nq + C::BR * C::NQT - 1) / (C::BR * C::NQT);
+  p.BH = a.BH;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.kv_per_split = a.kv_per_split;
+  p.n_split = a.n_split;
+  p.ws_o = a.ws_o;
+  p.ws_ml = a.ws_ml;
   p.c = a.c;
   p.tau = a.tau;
   p.fault = a.fault;
-  const long long grid = static_cast<long long>(p.n_qblk) * a.BH;
+  if (a.n_split < 1 || a.kv_per_split < C::BC || a.kv_per_split % C::BC != 0 ||
+      static_cast<long long>(a.n_split - 1) * a.kv_per_split >= a.Nk)
+    return cudaErrorInvalidValue;  // every split must own at least one key
+  const long long grid = static_cast<long long>(p.n_qblk) * a.BH * a.n_split;
   if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   fa_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream>>>(*a.tm_q, *a.tm_k,
                                                                                         *a.tm_v, p);

@@ -15,6 +15,11 @@ struct FwdLaunch {
   float* lse;               // [B, H, Nq] or nullptr
   int* err;                 // device error word
   int BH, Nq, Nk;
+  int H, Hkv;               // query heads per batch, key/value heads per batch (H % Hkv == 0)
+  int kv_per_split;         // keys per split, a multiple of the key tile (Nk rounded up when not split)
+  int n_split;              // key splits; > 1 writes partial states to ws_o / ws_ml for fa_fwd_merge
+  float* ws_o;              // [n_split][BH][Nq][d] fp32 unnormalised O
+  float* ws_ml;             // [n_split][BH][Nq][2] fp32 (m in log2 units, l)
   float c;                  // scale * log2(e)
   float tau;                // lazy-rescale threshold in log2 units (0 = rescale whenever m grows)
   int fault;                // test-only fault injection mode (0 = none)
@@ -23,19 +28,26 @@ struct FwdLaunch {
 
 // Tile geometry the tensor maps must be encoded with, per instantiation.
 struct FwdGeometry {
-  int box_cols;  // elements per 128-byte row segment (64 bf16, 32 fp32)
-  int q_rows;    // rows per Q box (128)
-  int kv_rows;   // rows per K box (the KV tile, Bc)
-  int v_kmajor;  // 1: V is read from a key-major copy [BH, d, Nk_pad] with boxes (32 keys, d rows)
+  int box_cols;     // elements per 128-byte row segment (64 bf16, 32 fp32)
+  int q_rows;       // rows per Q box (128)
+  int kv_rows;      // rows per K box (the KV tile, Bc)
+  int v_kmajor;     // 1: V is read from a key-major copy [BH, d, Nk_pad] with boxes (32 keys, d rows)
+  int rows_per_cta; // query rows one CTA covers
+  int ctas_per_sm;  // CTAs of this instantiation resident per SM
 };
 
 FwdGeometry fwd_geometry(int dtype_is_bf16, int d);
-int fwd_bc_bf16(int d);  // key-tile rows of the bf16 instantiation for head dim d
+FwdGeometry fwd_geometry_bf16(int d);
+
+// Merge of per-split partial states into O (dtype of the forward) and LSE:
+// O = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s; LSE = (M + log2 L) ln 2.
+cudaError_t launch_fwd_merge(const float* ws_o, const float* ws_ml, void* o, float* lse, long long rows, int d,
+                             int n_split, int out_bf16, cudaStream_t stream);
 
 // fp32 prep pass: qr = tf32(q), kr = tf32(k) (round to nearest), and the key-major copy
 // vt[bh][c][j] = tf32(v[bh][j][c]) for j < Nk, 0 for Nk <= j < Nk_pad.
 cudaError_t launch_prep_fp32(const float* q, const float* k, const float* v, float* qr, float* kr, float* vt,
-                             int BH, int Nq, int Nk, int Nk_pad, int d, cudaStream_t stream);
+                             int BH, int BHkv, int Nq, int Nk, int Nk_pad, int d, cudaStream_t stream);
 cudaError_t launch_fwd_bf16_d64(const FwdLaunch& a);
 cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a);
 cudaError_t launch_fwd_fp32_d64(const FwdLaunch& a);

@@ -58,9 +58,11 @@ typedef enum {
  *   dtype FA_BF16: bf16 operands, fp32 accumulation, P rounded to bf16 for P V.
  *   dtype FA_FP32: fp32 operands multiplied as TF32, P kept at TF32.  A prep
  *     pass first writes tf32-rounded (nearest) copies of Q and K and a
- *     key-major tf32 copy of V (tf32 tensor-core operands must be K-major)
- *     into a stream-ordered workspace of about 4*B*H*d*(Nq + 2*Nk) bytes
- *     (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *     key-major tf32 copy of V (tf32 tensor-core operands must be K-major).
+ *   When the query tiles cannot fill the GPU (small B*H*Nq) the keys are also
+ *   split across CTAs and merged (see fa_fwd_ex).  Any workspace these need
+ *   (fa_fwd_workspace_bytes) is taken stream-ordered (cudaMallocAsync /
+ *   cudaFreeAsync on `stream`).
  *   d must be 64 or 128; Nq, Nk >= 1 (ragged tails are masked); B, H >= 1;
  *   scale must be finite (1/sqrt(d) is the usual value; 1 reproduces [T4]-style
  *   unscaled scores).  Returns FA_OK or an fa_status code.
@@ -68,6 +70,35 @@ typedef enum {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int Nq, int Nk, int d, float scale, int dtype,
            fa_stream_t stream);
+
+/*
+ * fa_fwd_ex -- fa_fwd with every option exposed.  fa_fwd(...) is
+ * fa_fwd_ex(..., Hkv = H, causal = 0, kv_splits = 0, workspace = NULL, 0, stream).
+ *   Hkv        key/value heads per batch (grouped-query attention): k and v are
+ *              [B, Hkv, Nk, d]; query head h reads key/value head h / (H / Hkv).
+ *              H must be a multiple of Hkv (Hkv = H: plain multi-head).
+ *   causal     must be 0 (a causal mask is not provided yet: FA_ERR_UNSUPPORTED).
+ *   kv_splits  0 = automatic; 1 = one pass over all keys per query tile;
+ *              n > 1 = the keys are cut into n ranges handled by separate CTAs,
+ *              each writing an fp32 partial state (m, l, unnormalised O) that a
+ *              merge kernel combines ([T3] demo 2, split-KV / flash-decoding
+ *              applied to every query row).  Automatic splitting is used only
+ *              when the query tiles alone cannot fill the GPU.  n may not exceed
+ *              the number of key tiles (FA_ERR_INVALID_ARG).
+ *   workspace  device buffer of at least fa_fwd_workspace_bytes(...) bytes,
+ *              16-byte aligned, or NULL to allocate it stream-ordered.  Needed
+ *              by the fp32 path (rounded / transposed operand copies) and by
+ *              split runs; a bf16 call with one split needs none.
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+              int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int dtype,
+              int causal, int kv_splits, void* workspace, size_t workspace_bytes,
+              fa_stream_t stream);
+
+/* Bytes of workspace fa_fwd_ex needs for these arguments (kv_splits = 0 asks the
+ * current device's SM count); 0 when none is needed or the arguments are invalid. */
+size_t fa_fwd_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype,
+                              int causal, int kv_splits);
 
 /*
  * fa_decode_splitkv -- attention of one bf16 query per head over Nk keys,

@@ -106,9 +106,18 @@ def attention(q, k, v, scale: float):
     """Exact attention on [..., N, d] inputs; returns (O, LSE) as float64 arrays.
 
     Leading dimensions (batch, heads) must agree between q, k and v; each head
-    is independent.  LSE has shape [..., Nq].
+    is independent.  LSE has shape [..., Nq].  With 4-D inputs k and v may
+    have fewer heads Hkv than q (grouped-query attention): query head h then
+    uses key/value head h // (H / Hkv), i.e. consecutive query heads share one
+    key/value head.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim == 4 and k.ndim == 4 and k.shape[1] != q.shape[1]:
+        if q.shape[1] % k.shape[1] != 0:
+            raise ValueError("query heads must be a multiple of key/value heads")
+        group = q.shape[1] // k.shape[1]
+        k = np.ascontiguousarray(np.repeat(k, group, axis=1))
+        v = np.ascontiguousarray(np.repeat(v, group, axis=1))
     if q.ndim < 2 or k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
         raise ValueError("shape mismatch")
     lead = q.shape[:-2]

@@ -95,6 +95,8 @@ def tf32_score_bound(q, k, scale: float) -> np.ndarray:
     """Per query row, max over keys of 2u |scale| sum_i |q_i k_i| with u = 2^-11 (tf32 rounding of q and k)."""
     qa = np.abs(q.float().cpu().numpy().astype(np.float64))
     ka = np.abs(k.float().cpu().numpy().astype(np.float64))
+    if ka.shape[1] != qa.shape[1]:  # grouped-query heads
+        ka = np.repeat(ka, qa.shape[1] // ka.shape[1], axis=1)
     per_key = np.einsum("bhqd,bhkd->bhqk", qa, ka)
     return 2.0 * 2.0 ** -11 * abs(scale) * per_key.max(axis=-1) * 1.001
 

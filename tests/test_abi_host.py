@@ -137,3 +137,37 @@ def test_library_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def _fwd_ex(**kw):
+    a = dict(q=P, k=P, v=P, o=P2, lse=None, B=1, H=4, Hkv=2, Nq=16, Nk=256, d=64, scale=0.125, dtype=fa.FA_BF16,
+             causal=0, kv_splits=1, ws=None, ws_bytes=0)
+    a.update(kw)
+    return fa.lib().fa_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"], a["Nq"], a["Nk"],
+                              a["d"], a["scale"], a["dtype"], a["causal"], a["kv_splits"], a["ws"], a["ws_bytes"],
+                              None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hkv=3), fa.FA_ERR_INVALID_ARG),          # 4 query heads cannot share 3 key/value heads
+    (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=1), fa.FA_ERR_UNSUPPORTED),
+    (dict(kv_splits=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(kv_splits=5), fa.FA_ERR_INVALID_ARG),    # 256 keys are 4 bf16 d=64 key tiles of 64
+    (dict(ws=P + 4, kv_splits=2), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(v=None), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_ex_rejects(kw, status):
+    assert _fwd_ex(**kw) == status
+
+
+def test_fwd_workspace_bytes_explicit_splits():
+    L = fa.lib()
+    # bf16, one split: no workspace
+    assert L.fa_fwd_workspace_bytes(1, 4, 2, 100, 256, 64, fa.FA_BF16, 0, 1) == 0
+    # bf16, 2 splits: fp32 O (2*4*100*64*4 = 204800) + (m, l) (2*4*100*2*4 = 6400, a multiple of 256)
+    assert L.fa_fwd_workspace_bytes(1, 4, 2, 100, 256, 64, fa.FA_BF16, 0, 2) == 204800 + 6400
+    # fp32, one split: rounded Q (1*4*100*64*4 = 102400), rounded K (1*2*256*64*4), V^T (1*2*64*256*4)
+    assert L.fa_fwd_workspace_bytes(1, 4, 2, 100, 256, 64, fa.FA_FP32, 0, 1) == 102400 + 131072 + 131072
+    assert L.fa_fwd_workspace_bytes(1, 4, 3, 100, 256, 64, fa.FA_BF16, 0, 1) == 0  # invalid heads

@@ -24,10 +24,10 @@ def test_skipped_copy_times_out_then_recovers(cuda_device, d):
     sc = 1 / math.sqrt(d)
     assert fa.fa_check_device_error() == fa.FA_OK
     assert fa.fa_debug_set_fault(1) == fa.FA_OK
-    fa.fa_fwd(q, k, v, scale=sc)                      # enqueued fine; gives up on the device
+    fa.fa_fwd(q, k, v, scale=sc, kv_splits=1)         # enqueued fine; gives up on the device
     assert fa.fa_check_device_error() == fa.FA_ERR_TIMEOUT
     assert fa.fa_check_device_error() == fa.FA_OK     # the word was cleared
-    o, lse = fa.fa_fwd(q, k, v, scale=sc)             # the fault was one-shot
+    o, lse = fa.fa_fwd(q, k, v, scale=sc, kv_splits=1)  # the fault was one-shot
     torch.cuda.synchronize()
     assert fa.fa_check_device_error() == fa.FA_OK
     check_fwd(q, k, v, o, lse, sc, name=f"after fault d{d}")

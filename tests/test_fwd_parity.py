@@ -82,24 +82,68 @@ def test_lse_optional_and_stream(cuda_device):
     assert torch.equal(o1, o2)
 
 
-@pytest.mark.parametrize("dtype,limit", [("bf16", 1 << 20), ("fp32", 16 << 20)])
-def test_no_quadratic_memory(cuda_device, dtype, limit):
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("kv_splits", [1, 0])
+def test_no_quadratic_memory(cuda_device, dtype, kv_splits):
     """No Nq x Nk buffer is ever allocated ([T1] §4.2: peak HBM 130 MB standard vs ~1 MB tiled at N=4096).
 
-    bf16 allocates nothing; fp32 takes an O(N d) prep workspace (3 MiB here), far below the 64 MiB
-    one N x N fp32 matrix would need."""
-    q, k, v = make_qkv(1, 1, 4096, 4096, 64, dtype, seed=3, device=cuda_device)
+    A bf16 call with one key split allocates nothing.  The fp32 prep copies and split-KV partial
+    states are O(N d * splits): the workspace the library reports, below half of the 64 MiB of one
+    N x N fp32 matrix (standard attention holds two: S and P)."""
+    N = 4096
+    q, k, v = make_qkv(1, 1, N, N, 64, dtype, seed=3, device=cuda_device)
     o = torch.empty_like(q)
-    lse = torch.empty((1, 1, 4096), device=cuda_device)
+    lse = torch.empty((1, 1, N), device=cuda_device)
+    ws = fa.fa_fwd_workspace_bytes(1, 1, 1, N, N, 64, q.dtype, kv_splits=kv_splits)
+    if dtype == "bf16" and kv_splits == 1:
+        assert ws == 0
+    assert ws <= N * N * 4 // 2
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     torch.cuda.reset_peak_memory_stats()
     base = torch.cuda.memory_allocated()
-    fa.fa_fwd(q, k, v, o=o, lse=lse)
+    fa.fa_fwd(q, k, v, o=o, lse=lse, kv_splits=kv_splits)
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert torch.cuda.max_memory_allocated() - base <= 1 << 20
-    assert free0 - free1 <= limit  # nothing large allocated behind torch's back either
+    assert free0 - free1 <= ws + (2 << 20)  # nothing else allocated behind torch's back
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kv_splits", [1, 2, 5, 0])
+def test_kv_splits(cuda_device, dtype, d, kv_splits):
+    """Keys cut into ranges handled by separate CTAs and merged from (m, l, O) partial states
+    ("CS349E 第 11 讲 01_online_softmax.py", demo 2): ragged last range, every split count."""
+    q, k, v = make_qkv(1, 2, 300, 700, d, dtype, seed=600 + d + kv_splits, device=cuda_device)
+    sc = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd(q, k, v, scale=sc, kv_splits=kv_splits)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    check_fwd(q, k, v, o, lse, sc, name=f"{dtype} d{d} kv_splits={kv_splits}")
+
+
+def test_split_caller_workspace(cuda_device):
+    q, k, v = make_qkv(2, 2, 257, 1000, 64, "bf16", seed=31, device=cuda_device)
+    n = fa.fa_fwd_workspace_bytes(2, 2, 2, 257, 1000, 64, torch.bfloat16, kv_splits=4)
+    ws = torch.empty(n // 4 + 4, device=cuda_device, dtype=torch.float32)
+    o1, l1 = fa.fa_fwd(q, k, v, kv_splits=4, workspace=ws)
+    o2, l2 = fa.fa_fwd(q, k, v, kv_splits=4)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    check_fwd(q, k, v, o1, l1, 1 / 8, name="split caller workspace")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("H,Hkv,d", [(8, 2, 64), (4, 1, 128), (6, 3, 64)])
+def test_grouped_query_heads(cuda_device, dtype, H, Hkv, d):
+    """Query head h reads key/value head h // (H / Hkv) (grouped-query / multi-query attention)."""
+    q, _, _ = make_qkv(2, H, 200, 1, d, dtype, seed=700 + H, device=cuda_device)
+    _, k, v = make_qkv(2, Hkv, 1, 333, d, dtype, seed=800 + Hkv, device=cuda_device)
+    sc = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd(q, k, v, scale=sc)
+    torch.cuda.synchronize()
+    check_fwd(q, k, v, o, lse, sc, name=f"{dtype} gqa H={H} Hkv={Hkv} d{d}")
 
 
 def test_deterministic(cuda_device):

@@ -275,3 +275,16 @@ def test_peaked_scores_tiled():
     o, lse = forms.attention_tiled(q, k, v, 128, 128, sc)
     assert np.abs(o - ref).max() <= 1e-13
     assert np.abs(lse - ref_lse).max() <= 1e-12
+
+
+def test_grouped_query_heads_library():
+    """Grouped-query attention (query head h reads key/value head h // group) against torch's
+    float64 SDPA with enable_gqa, and Hkv = H reduces to plain multi-head attention."""
+    rng = np.random.default_rng(14)
+    q, k, v = _rand(rng, 2, 6, 5, 8), _rand(rng, 2, 2, 9, 8), _rand(rng, 2, 2, 9, 8)
+    o, lse = oracle.attention(q, k, v, 0.3)
+    t = [torch.tensor(x) for x in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(*t, scale=0.3, enable_gqa=True).numpy()
+    assert np.abs(o - ref).max() <= 1e-14
+    o1, _ = oracle.attention(q[:, :3], k[:, :1].repeat(3, axis=1), v[:, :1].repeat(3, axis=1), 0.3)
+    assert np.array_equal(o1, o[:, :3])
