@@ -69,6 +69,10 @@ def _load():
             lib.fao_attention.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
                                           ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double]
             lib.fao_attention.restype = ctypes.c_int
+            lib.fao_attention_head_limits.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                                      ctypes.c_long, ctypes.c_double,
+                                                      ctypes.POINTER(ctypes.c_long)]
+            lib.fao_attention_head_limits.restype = ctypes.c_int
             lib.fao_partial_state.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
                                               ctypes.c_double, _dp, _dp, _dp]
             lib.fao_partial_state.restype = ctypes.c_int
@@ -102,7 +106,18 @@ def _check(rc: int, what: str) -> None:
         raise ValueError(f"oracle {what} failed with code {rc}")
 
 
-def attention(q, k, v, scale: float):
+def causal_limits(rows, nq_total: int, nk: int) -> np.ndarray:
+    """Visible keys per query row under a causal mask aligned to the bottom-right corner.
+
+    Query row i (of nq_total) sees keys 0 .. i + (nk - nq_total): the last query sees every key,
+    and with nq_total == nk this is the usual lower triangle.  Requires nq_total <= nk.
+    """
+    if nq_total > nk:
+        raise ValueError("causal attention needs Nq <= Nk")
+    return np.asarray(rows, dtype=np.int64) + (nk - nq_total) + 1
+
+
+def attention(q, k, v, scale: float, causal: bool = False, rows=None, nq_total=None):
     """Exact attention on [..., N, d] inputs; returns (O, LSE) as float64 arrays.
 
     Leading dimensions (batch, heads) must agree between q, k and v; each head
@@ -110,8 +125,14 @@ def attention(q, k, v, scale: float):
     have fewer heads Hkv than q (grouped-query attention): query head h then
     uses key/value head h // (H / Hkv), i.e. consecutive query heads share one
     key/value head.
+
+    causal: each query row only sees keys up to its causal limit (see
+    causal_limits).  When q holds a subset of the query rows, `rows` gives
+    their indices and `nq_total` the full query length.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
+    if causal:
+        return _attention_causal(q, k, v, scale, rows, nq_total)
     if q.ndim == 4 and k.ndim == 4 and k.shape[1] != q.shape[1]:
         if q.shape[1] % k.shape[1] != 0:
             raise ValueError("query heads must be a multiple of key/value heads")
@@ -129,6 +150,32 @@ def attention(q, k, v, scale: float):
     _check(_load().fao_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), 1, bh, nq, nk, d,
                                  float(scale)), "attention")
     return o, lse
+
+
+def _attention_causal(q, k, v, scale, rows, nq_total):
+    if q.ndim == 4 and k.ndim == 4 and k.shape[1] != q.shape[1]:
+        group = q.shape[1] // k.shape[1]
+        k = np.ascontiguousarray(np.repeat(k, group, axis=1))
+        v = np.ascontiguousarray(np.repeat(v, group, axis=1))
+    lead = q.shape[:-2]
+    nq, d = q.shape[-2:]
+    nk = k.shape[-2]
+    if rows is None:
+        rows = np.arange(nq)
+    limits = np.ascontiguousarray(causal_limits(rows, nq if nq_total is None else nq_total, nk), dtype=np.int64)
+    lim_p = limits.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+    qf, kf, vf = q.reshape(-1, nq, d), k.reshape(-1, nk, d), v.reshape(-1, nk, d)
+    o = np.empty_like(qf)
+    lse = np.empty(qf.shape[:2], dtype=np.float64)
+    L = _load()
+    for h in range(qf.shape[0]):
+        qh, kh, vh = (np.ascontiguousarray(x[h]) for x in (qf, kf, vf))
+        oh = np.empty((nq, d))
+        lh = np.empty(nq)
+        _check(L.fao_attention_head_limits(_ptr(qh), _ptr(kh), _ptr(vh), _ptr(oh), _ptr(lh), nq, nk, d,
+                                           float(scale), lim_p), "attention (causal)")
+        o[h], lse[h] = oh, lh
+    return o.reshape(lead + (nq, d)), lse.reshape(lead + (nq,))
 
 
 def partial_state(q, k, v, scale: float):

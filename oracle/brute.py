@@ -11,8 +11,11 @@ from __future__ import annotations
 import numpy as np
 
 
-def attention_mp(q, k, v, scale: float, digits: int = 50):
-    """Returns (O, LSE) as float64 arrays for one head: q [nq, d], k/v [nk, d]."""
+def attention_mp(q, k, v, scale: float, digits: int = 50, limits=None):
+    """Returns (O, LSE) as float64 arrays for one head: q [nq, d], k/v [nk, d].
+
+    limits[i], if given, is the number of leading keys query row i may see.
+    """
     import mpmath as mp
 
     q = np.asarray(q, dtype=np.float64)
@@ -28,9 +31,10 @@ def attention_mp(q, k, v, scale: float, digits: int = 50):
         vv = [[mp.mpf(float(x)) for x in row] for row in v]
         for i in range(nq):
             qi = [mp.mpf(float(x)) for x in q[i]]
-            e = [mp.exp(sc * mp.fsum(a * b for a, b in zip(qi, kk[j]))) for j in range(nk)]
+            n_i = nk if limits is None else int(limits[i])
+            e = [mp.exp(sc * mp.fsum(a * b for a, b in zip(qi, kk[j]))) for j in range(n_i)]
             z = mp.fsum(e)
             for c in range(v.shape[1]):
-                o[i, c] = float(mp.fsum(e[j] * vv[j][c] for j in range(nk)) / z)
+                o[i, c] = float(mp.fsum(e[j] * vv[j][c] for j in range(n_i)) / z)
             lse[i] = float(mp.log(z))
     return o, lse

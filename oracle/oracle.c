@@ -98,6 +98,29 @@ int fao_attention_head(const double* q, const double* k, const double* v,
 }
 
 /*
+ * Exact attention for one head where query row i sees only its first
+ * limits[i] keys (1 <= limits[i] <= nk): the softmax runs over keys
+ * 0 .. limits[i]-1 only.  A causal mask is one choice of limits.
+ */
+int fao_attention_head_limits(const double* q, const double* k, const double* v,
+                              double* o, double* lse, long nq, long nk, long d,
+                              double scale, const long* limits)
+{
+    if (nq < 0 || nk < 1 || d < 1 || !limits) return FAO_BAD_ARG;
+    if (nq == 0) return FAO_OK;
+    if (!q || !k || !v || !o) return FAO_BAD_ARG;
+    for (long i = 0; i < nq; ++i)
+        if (limits[i] < 1 || limits[i] > nk) return FAO_BAD_ARG;
+    double* s = (double*)malloc((size_t)nk * sizeof(double));
+    if (!s) return FAO_NO_MEM;
+    for (long i = 0; i < nq; ++i)
+        attention_row_3pass(q + i * d, k, v, o + i * d, lse ? lse + i : NULL,
+                            limits[i], d, scale, s);
+    free(s);
+    return FAO_OK;
+}
+
+/*
  * Exact attention over [B, H, N, d] contiguous tensors (each head on its own).
  * lse is [B, H, nq] or NULL.
  */

@@ -288,3 +288,43 @@ def test_grouped_query_heads_library():
     assert np.abs(o - ref).max() <= 1e-14
     o1, _ = oracle.attention(q[:, :3], k[:, :1].repeat(3, axis=1), v[:, :1].repeat(3, axis=1), 0.3)
     assert np.array_equal(o1, o[:, :3])
+
+
+@pytest.mark.parametrize("nq,nk", [(9, 9), (5, 12), (1, 7)])
+def test_causal_brute_force(nq, nk):
+    """Causal mask aligned to the bottom-right corner (row i sees keys 0 .. i + Nk - Nq) against the
+    50-digit brute force restricted to the same keys."""
+    brute = pytest.importorskip("oracle.brute")
+    pytest.importorskip("mpmath")
+    rng = np.random.default_rng(nq * 10 + nk)
+    q, k, v = _rand(rng, nq, 6), _rand(rng, nk, 6), _rand(rng, nk, 6)
+    o, lse = oracle.attention(q[None, None], k[None, None], v[None, None], 0.4, causal=True)
+    lim = oracle.causal_limits(np.arange(nq), nq, nk)
+    ob, lb = brute.attention_mp(q, k, v, 0.4, limits=lim)
+    assert np.abs(o[0, 0] - ob).max() <= 1e-14
+    assert np.abs(lse[0, 0] - lb).max() <= 1e-13
+
+
+def test_causal_library_and_closed_forms():
+    """torch's float64 SDPA with is_causal (square case) and with an explicit bottom-right mask;
+    with Nq == Nk the first row is v_0 with LSE = s_00 and the last row is unmasked attention."""
+    rng = np.random.default_rng(15)
+    q, k, v = _rand(rng, 2, 3, 10, 8), _rand(rng, 2, 3, 10, 8), _rand(rng, 2, 3, 10, 8)
+    o, lse = oracle.attention(q, k, v, 0.3, causal=True)
+    t = [torch.tensor(x) for x in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(*t, scale=0.3, is_causal=True).numpy()
+    assert np.abs(o - ref).max() <= 1e-14
+    assert np.array_equal(o[:, :, 0], v[:, :, 0])
+    assert np.abs(lse[:, :, 0] - 0.3 * np.einsum("bhd,bhd->bh", q[:, :, 0], k[:, :, 0])).max() <= 1e-14
+    full, _ = oracle.attention(q, k, v, 0.3)
+    assert np.abs(o[:, :, -1] - full[:, :, -1]).max() <= 1e-15
+    # Nq < Nk: bottom-right alignment through an explicit boolean mask
+    q2 = _rand(rng, 1, 2, 4, 8)
+    o2, _ = oracle.attention(q2, k[:1, :2], v[:1, :2], 0.3, causal=True)
+    mask = torch.tensor(np.arange(10)[None, :] <= np.arange(4)[:, None] + 6)
+    ref2 = torch.nn.functional.scaled_dot_product_attention(torch.tensor(q2), t[1][:1, :2], t[2][:1, :2], scale=0.3,
+                                                            attn_mask=mask).numpy()
+    assert np.abs(o2 - ref2).max() <= 1e-14
+    # a subset of rows with their absolute indices gives the same rows
+    o3, _ = oracle.attention(q[:, :, [2, 7]], k, v, 0.3, causal=True, rows=[2, 7], nq_total=10)
+    assert np.array_equal(o3, o[:, :, [2, 7]])
