@@ -15,6 +15,12 @@ def fwd_flops(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
     return 4 * B * H * Nq * Nk * d
 
 
+def fwd_flops_causal(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    """FLOPs of the two contractions under a bottom-right causal mask: row i sees i + Nk - Nq + 1 keys."""
+    visible = Nq * (Nk - Nq) + Nq * (Nq + 1) // 2
+    return 4 * B * H * visible * d
+
+
 def fwd_min_bytes(B: int, H: int, Nq: int, Nk: int, d: int, dtype: str) -> int:
     """Smallest HBM traffic of one forward: read Q, K, V once, write O and the fp32 LSE."""
     e = ESIZE[dtype]

@@ -134,7 +134,8 @@ int plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype, int causal
   if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (causal != 0) return FA_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;  // the first Nq - Nk rows would see no key
   if (kv_splits < 0) return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
@@ -268,6 +269,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.n_split = pl.n_split;
   a.ws_o = pl.n_split > 1 ? reinterpret_cast<float*>(ws + pl.off_wo) : nullptr;
   a.ws_ml = pl.n_split > 1 ? reinterpret_cast<float*>(ws + pl.off_wml) : nullptr;
+  a.causal = causal;
   a.c = scale * 1.4426950408889634f;
   a.tau = 8.0f;
   a.fault = g_fault.exchange(0);

@@ -110,6 +110,8 @@ struct FwdParams {
   int n_split;          // 1: write O and LSE; > 1: write unnormalised partial states for the merge
   float* ws_o;          // [n_split][BH][Nq][D] fp32 unnormalised O (split mode)
   float* ws_ml;         // [n_split][BH][Nq][2] fp32 (m in log2 units, l) (split mode)
+  int causal;           // 1: query row i sees keys j <= i + causal_off only
+  int causal_off;       // Nk - Nq (mask aligned to the bottom-right corner)
   float c, tau;
   int fault;
 };
@@ -200,15 +202,19 @@ __global__ void __maxnreg__(C::MAXREG)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // blockIdx.x = (split * BH + bh) * n_qblk + qb: CTAs sharing a head and key range are adjacent
-  const int qb = blockIdx.x % p.n_qblk;
+  // blockIdx.x = (split * BH + bh) * n_qblk + qb: CTAs sharing a head and key range are adjacent.
+  // With a causal mask the query blocks run last-to-first, so the longest CTAs start first.
+  const int qb = p.causal ? p.n_qblk - 1 - static_cast<int>(blockIdx.x % p.n_qblk)
+                          : static_cast<int>(blockIdx.x % p.n_qblk);
   const int bh = (blockIdx.x / p.n_qblk) % p.BH;
   const int split = blockIdx.x / (p.n_qblk * p.BH);
   const int kvh = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);  // key/value head of this query head
   const int q0 = qb * C::BR * C::NQT;
   const int k_begin = split * p.kv_per_split;
   const int k_end = min(p.Nk, k_begin + p.kv_per_split);  // the host makes every split non-empty
-  const int T = (k_end - k_begin + C::BC - 1) / C::BC;
+  // keys past the causal limit of the CTA's last row are never loaded or multiplied
+  const int k_hi = p.causal ? min(k_end, q0 + C::NQT * C::BR + p.causal_off) : k_end;
+  const int T = k_hi > k_begin ? (k_hi - k_begin + C::BC - 1) / C::BC : 0;  // 0 only in split mode
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_q = bar0;
@@ -255,7 +261,7 @@ __global__ void __maxnreg__(C::MAXREG)
 
   if (warp == C::LOAD_WARP) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && T > 0) {
       int nk_done = 0, nv_done = 0;  // key tiles whose K (resp. V) copy was issued: tiles 0 .. n-1
       mbar_expect_tx(bar_q, C::NQT * C::Q_BYTES);
 #pragma unroll
@@ -352,7 +358,7 @@ __global__ void __maxnreg__(C::MAXREG)
         if (elect_one()) mma_commit(bar);
         __syncwarp();
       };
-      bool ok = wait_all(bar_q, 0, W_Q) && wait_all(bar_kf(0), 0, W_KF);
+      bool ok = T > 0 && wait_all(bar_q, 0, W_Q) && wait_all(bar_kf(0), 0, W_KF);
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -406,6 +412,8 @@ __global__ void __maxnreg__(C::MAXREG)
     const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::D + h * C::OCOLS;
     float* xch = reinterpret_cast<float*>(smem + C::OFF_XCHG);
     auto xidx = [&](int slot, int hh) { return ((slot * C::NQT + t) * C::SPLIT + hh) * 128 + row; };
+    // keys this row may see in the CTA's range: [k_begin, row_lim)
+    const int row_lim = p.causal ? min(k_end, q0 + t * C::BR + row + 1 + p.causal_off) : k_end;
     const float c = p.c;
     float m_ref = -INFINITY;
     float l = 0.f;
@@ -415,7 +423,7 @@ __global__ void __maxnreg__(C::MAXREG)
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
       okw = __all_sync(0xffffffffu, okw);
       uint32_t sr[C::COLS / 32][32];
-      const int valid = k_end - k_begin - j * C::BC - h * C::COLS;  // valid key columns here (may be <= 0)
+      const int valid = row_lim - k_begin - j * C::BC - h * C::COLS;  // valid key columns here (may be <= 0)
       float m_part = -INFINITY;
       {  // loaded even when the wait gave up (then the values are stale and unused): a conditional
          // load would keep the row in local memory
@@ -504,7 +512,7 @@ __global__ void __maxnreg__(C::MAXREG)
       l = l * alpha + ((r0 + r1) + (r2 + r3));
     }
     // ---------------------------------------------------------- epilogue: O / l, LSE
-    if (ok) {  // `ok` agrees across the warpgroups of the tile here
+    if (ok && T > 0) {  // `ok` agrees across the warpgroups of the tile here
       bool okw = mbar_wait(bar_od(t), 0, abort_flag, p.err, W_OD);
       okw = __all_sync(0xffffffffu, okw);
       if constexpr (C::SPLIT > 1) {  // total row sum from the partial sums (slot T & 1 is free)
@@ -518,7 +526,16 @@ __global__ void __maxnreg__(C::MAXREG)
         ok = okw;
       }
     }
-    if (ok && p.n_split > 1) {  // partial state (m, l, unnormalised O) of this key range, for the merge
+    if (T == 0) {  // split mode, key range entirely above the causal diagonal: empty state (-inf, 0, 0)
+      const int qrow = q0 + t * C::BR + row;
+      if (qrow < p.Nq) {
+        const size_t srow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + qrow;
+        float* wrow = p.ws_o + srow * C::D + h * C::OCOLS;
+#pragma unroll
+        for (int c4 = 0; c4 < C::OCOLS / 4; ++c4) reinterpret_cast<uint4*>(wrow)[c4] = make_uint4(0, 0, 0, 0);
+        if (h == 0) reinterpret_cast<float2*>(p.ws_ml)[srow] = make_float2(-INFINITY, 0.f);
+      }
+    } else if (ok && p.n_split > 1) {  // partial state (m, l, unnormalised O) of this key range, for the merge
       tc_fence_after();
       const int qrow = q0 + t * C::BR + row;
       const bool in_range = qrow < p.Nq;
@@ -610,6 +627,9 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   p.n_split = a.n_split;
   p.ws_o = a.ws_o;
   p.ws_ml = a.ws_ml;
+  p.causal = a.causal;
+  p.causal_off = a.Nk - a.Nq;
+  if (a.causal && (a.Nq > a.Nk || a.n_split < 1)) return cudaErrorInvalidValue;
   p.c = a.c;
   p.tau = a.tau;
   p.fault = a.fault;

@@ -20,6 +20,7 @@ struct FwdLaunch {
   int n_split;              // key splits; > 1 writes partial states to ws_o / ws_ml for fa_fwd_merge
   float* ws_o;              // [n_split][BH][Nq][d] fp32 unnormalised O
   float* ws_ml;             // [n_split][BH][Nq][2] fp32 (m in log2 units, l)
+  int causal;               // 1: query row i sees keys j <= i + Nk - Nq (requires Nq <= Nk)
   float c;                  // scale * log2(e)
   float tau;                // lazy-rescale threshold in log2 units (0 = rescale whenever m grows)
   int fault;                // test-only fault injection mode (0 = none)

@@ -27,6 +27,7 @@ def main(argv=None) -> int:
     ap.add_argument("--B", type=int, default=0)
     ap.add_argument("--H", type=int, default=0)
     ap.add_argument("--time", action="store_true", help="time the launches with CUDA events and print the rate")
+    ap.add_argument("--causal", action="store_true", help="causal mask (prefill workloads)")
     a = ap.parse_args(argv)
     w = WORKLOADS[a.workload]
     if a.B:
@@ -43,7 +44,7 @@ def main(argv=None) -> int:
         if w.splits:
             fa.fa_decode_splitkv_ex(q, k, v, w.splits, merge_order=order)
         else:
-            fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse)
+            fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse, causal=a.causal)
 
     torch.cuda.synchronize()
     run()
@@ -57,6 +58,8 @@ def main(argv=None) -> int:
         ms = start.elapsed_time(end) / a.launches
         if w.splits:
             rate = f"{accounting.decode_min_bytes(w.B, w.H, w.Nk, w.d) / ms / 1e6:.1f} GB/s"
+        elif a.causal:
+            rate = f"{accounting.fwd_flops_causal(w.B, w.H, w.Nq, w.Nk, w.d) / ms / 1e9:.1f} TFLOP/s (causal)"
         else:
             rate = f"{accounting.fwd_flops(w.B, w.H, w.Nq, w.Nk, w.d) / ms / 1e9:.1f} TFLOP/s"
         print(f"time: {w.name} {ms * 1e3:.1f} us/launch {rate}")

@@ -77,7 +77,11 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   Hkv        key/value heads per batch (grouped-query attention): k and v are
  *              [B, Hkv, Nk, d]; query head h reads key/value head h / (H / Hkv).
  *              H must be a multiple of Hkv (Hkv = H: plain multi-head).
- *   causal     must be 0 (a causal mask is not provided yet: FA_ERR_UNSUPPORTED).
+ *   causal     1 = causal mask aligned to the bottom-right corner: query row i
+ *              sees keys 0 .. i + (Nk - Nq), so the last query sees every key
+ *              and Nq == Nk gives the usual lower triangle ([T1] §7 names the
+ *              extension).  Requires Nq <= Nk (FA_ERR_INVALID_ARG otherwise).
+ *              Key tiles above the diagonal are skipped, not just masked.
  *   kv_splits  0 = automatic; 1 = one pass over all keys per query tile;
  *              n > 1 = the keys are cut into n ranges handled by separate CTAs,
  *              each writing an fp32 partial state (m, l, unnormalised O) that a

@@ -53,7 +53,7 @@ def sample_rows(Nq: int, n_random: int, seed: int, tile: int = 128, n_tiles: int
     return np.array(sorted(rows), dtype=np.int64)
 
 
-def check_fwd(q, k, v, o, lse, scale: float, rows=None, name: str = "") -> dict:
+def check_fwd(q, k, v, o, lse, scale: float, rows=None, name: str = "", causal: bool = False) -> dict:
     """Compares GPU outputs (o, lse) with the oracle on all rows or on `rows`; asserts the tolerances."""
     dt = dtype_name(q)
     if rows is None:
@@ -62,7 +62,7 @@ def check_fwd(q, k, v, o, lse, scale: float, rows=None, name: str = "") -> dict:
         idx = torch.as_tensor(rows, device=q.device)
         qs, og = q[:, :, idx], o[:, :, idx]
         lg = lse[:, :, idx] if lse is not None else None
-    ref_o, ref_lse = oracle.attention(qs, k, v, scale)
+    ref_o, ref_lse = oracle.attention(qs, k, v, scale, causal=causal, rows=rows, nq_total=q.shape[2])
     got = og.float().cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all(), f"{name}: non-finite output"
     err = np.abs(got - ref_o)

@@ -151,7 +151,8 @@ def _fwd_ex(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(Hkv=3), fa.FA_ERR_INVALID_ARG),          # 4 query heads cannot share 3 key/value heads
     (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
-    (dict(causal=1), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=1, Nq=300, Nk=256), fa.FA_ERR_INVALID_ARG),  # rows 0..43 would see no key
     (dict(kv_splits=-1), fa.FA_ERR_INVALID_ARG),
     (dict(kv_splits=5), fa.FA_ERR_INVALID_ARG),    # 256 keys are 4 bf16 d=64 key tiles of 64
     (dict(ws=P + 4, kv_splits=2), fa.FA_ERR_INVALID_ARG),
