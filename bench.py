@@ -45,6 +45,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded oracle sample for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the causal / GQA / split-KV measurements")
     return ap.parse_args()
 
 
@@ -383,6 +384,8 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
     }
+    if not args.no_extras:
+        line["extras"] = measure_extras(fa, torch, accounting, dev, stream)
     if not args.no_cpu_baseline:
         cb_pre, cb_dec = cpu_baseline(args.cpu_seconds)
         line["cpu_baseline"] = cb_pre
@@ -391,6 +394,49 @@ def run_gpu(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def measure_extras(fa, torch, accounting, dev, stream, launches=20):
+    """Rates of the extensions beyond the headline step, each timed alone with CUDA events on
+    `stream` after 3 warm-up launches (not part of `value`):
+      causal        the two bf16 prefill workloads with the causal mask (visible-key FLOPs)
+      gqa           B=4 H=16 N=4096 d=64 bf16 with 2 key/value heads
+      split_kv      B=1 H=1 N=4096 d=64 fp32 (TF32) with automatic key splits vs one split
+    """
+    from attention_forward_05_gb300.inputs import WORKLOADS, make_qkv, workload_inputs
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(launches):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / launches
+
+    out = {}
+    for name in PREFILL:
+        w = WORKLOADS[name]
+        q, k, v = workload_inputs(w, device=dev)
+        ms = timed(lambda: fa.fa_fwd(q, k, v, scale=w.scale, causal=True, stream=stream))
+        out[f"causal_{name}"] = {"ms": ms, "tflops": accounting.fwd_flops_causal(w.B, w.H, w.Nq, w.Nk, w.d) / ms / 1e9}
+        del q, k, v
+    w = WORKLOADS["mh_prefill"]
+    q, _, _ = make_qkv(w.B, w.H, w.Nq, 1, w.d, "bf16", seed=w.seed, device=dev)
+    _, k, v = make_qkv(w.B, 2, 1, w.Nk, w.d, "bf16", seed=w.seed + 1, device=dev)
+    ms = timed(lambda: fa.fa_fwd(q, k, v, scale=w.scale, stream=stream))
+    out["gqa_mh_prefill_hkv2"] = {"ms": ms, "tflops": accounting.fwd_flops(w.B, w.H, w.Nq, w.Nk, w.d) / ms / 1e9}
+    w = WORKLOADS["long_fp32"]
+    q, k, v = workload_inputs(w, device=dev)
+    fl = accounting.fwd_flops(w.B, w.H, w.Nq, w.Nk, w.d)
+    for tag, ks in (("split_kv_auto", 0), ("split_kv_off", 1)):
+        ms = timed(lambda: fa.fa_fwd(q, k, v, scale=w.scale, kv_splits=ks, stream=stream))
+        out[f"{tag}_long_fp32"] = {"ms": ms, "tflops": fl / ms / 1e9}
+    if fa.fa_check_device_error() != fa.FA_OK:
+        raise RuntimeError("device timeout in the extra measurements")
+    return out
 
 
 def measure_e2e(fa, torch, pre, dec, stream, steps, flops_step, dec_bytes):
