@@ -73,6 +73,9 @@ def _load():
                                                       ctypes.c_long, ctypes.c_double,
                                                       ctypes.POINTER(ctypes.c_long)]
             lib.fao_attention_head_limits.restype = ctypes.c_int
+            lib.fao_attention_bwd_head.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
+                                                   ctypes.c_long, ctypes.c_long, ctypes.c_double]
+            lib.fao_attention_bwd_head.restype = ctypes.c_int
             lib.fao_partial_state.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
                                               ctypes.c_double, _dp, _dp, _dp]
             lib.fao_partial_state.restype = ctypes.c_int
@@ -176,6 +179,27 @@ def _attention_causal(q, k, v, scale, rows, nq_total):
                                            float(scale), lim_p), "attention (causal)")
         o[h], lse[h] = oh, lh
     return o.reshape(lead + (nq, d)), lse.reshape(lead + (nq,))
+
+
+def attention_bwd(q, k, v, dout, scale: float):
+    """Gradients (dQ, dK, dV) of exact attention for a loss whose gradient w.r.t. O is dout.
+
+    q, dout [..., Nq, d]; k, v [..., Nk, d] with matching leading dimensions.  float64 arrays.
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    lead = q.shape[:-2]
+    nq, d = q.shape[-2:]
+    nk = k.shape[-2]
+    qf, kf, vf, gf = q.reshape(-1, nq, d), k.reshape(-1, nk, d), v.reshape(-1, nk, d), dout.reshape(-1, nq, d)
+    dq, dk, dv = np.empty_like(qf), np.empty_like(kf), np.empty_like(vf)
+    L = _load()
+    for h in range(qf.shape[0]):
+        a, b, c_, g = (np.ascontiguousarray(x[h]) for x in (qf, kf, vf, gf))
+        oq, ok_, ov = np.empty((nq, d)), np.empty((nk, d)), np.empty((nk, d))
+        _check(L.fao_attention_bwd_head(_ptr(a), _ptr(b), _ptr(c_), _ptr(g), _ptr(oq), _ptr(ok_), _ptr(ov), nq, nk,
+                                        d, float(scale)), "attention_bwd")
+        dq[h], dk[h], dv[h] = oq, ok_, ov
+    return dq.reshape(lead + (nq, d)), dk.reshape(lead + (nk, d)), dv.reshape(lead + (nk, d))
 
 
 def partial_state(q, k, v, scale: float):

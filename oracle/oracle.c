@@ -257,3 +257,73 @@ int fao_decode_splitkv(const double* q, const double* k, const double* v,
     free(acc_o);
     return rc;
 }
+
+/*
+ * Gradients of exact attention for one head, from the plain definition.
+ *   Forward:  S = scale Q K^T,  P = row-softmax(S),  O = P V.
+ *   Given dO (the gradient of a loss with respect to O):
+ *     dV = P^T dO                                  ([T2] Exercise 5: dV_j = sum_i P_ij^T dO_i)
+ *     dP = dO V^T
+ *     dS_ij = P_ij (dP_ij - D_i),  D_i = sum_c dO_ic O_ic   (softmax Jacobian, row by row)
+ *     dQ = scale dS K,   dK = scale dS^T Q
+ *   (the chain rule through S = scale Q K^T; the pages give only dV, the rest is calculus).
+ *   q, dq [nq, d]; k, v, dk, dv [nk, d]; dout [nq, d].  Plain loops, O(nq nk d).
+ */
+int fao_attention_bwd_head(const double* q, const double* k, const double* v,
+                           const double* dout, double* dq, double* dk, double* dv,
+                           long nq, long nk, long d, double scale)
+{
+    if (nq < 1 || nk < 1 || d < 1) return FAO_BAD_ARG;
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return FAO_BAD_ARG;
+    double* P = (double*)malloc((size_t)nq * nk * sizeof(double));
+    double* orow = (double*)malloc((size_t)d * sizeof(double));
+    if (!P || !orow) {
+        free(P);
+        free(orow);
+        return FAO_NO_MEM;
+    }
+    for (long i = 0; i < nq; ++i) { /* P row by row: scores, max, exp, normalise */
+        double* p = P + i * nk;
+        for (long j = 0; j < nk; ++j) {
+            double acc = 0.0;
+            for (long c = 0; c < d; ++c) acc += q[i * d + c] * k[j * d + c];
+            p[j] = scale * acc;
+        }
+        double m = p[0];
+        for (long j = 1; j < nk; ++j)
+            if (p[j] > m) m = p[j];
+        double l = 0.0;
+        for (long j = 0; j < nk; ++j) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        for (long j = 0; j < nk; ++j) p[j] /= l;
+    }
+    for (long x = 0; x < nq * d; ++x) dq[x] = 0.0;
+    for (long x = 0; x < nk * d; ++x) dk[x] = dv[x] = 0.0;
+    for (long i = 0; i < nq; ++i) {
+        const double* p = P + i * nk;
+        const double* go = dout + i * d;
+        /* O_i and D_i = <dO_i, O_i> */
+        for (long c = 0; c < d; ++c) orow[c] = 0.0;
+        for (long j = 0; j < nk; ++j)
+            for (long c = 0; c < d; ++c) orow[c] += p[j] * v[j * d + c];
+        double Di = 0.0;
+        for (long c = 0; c < d; ++c) Di += go[c] * orow[c];
+        for (long j = 0; j < nk; ++j) {
+            /* dV_j += P_ij dO_i */
+            for (long c = 0; c < d; ++c) dv[j * d + c] += p[j] * go[c];
+            /* dP_ij = <dO_i, V_j>,  dS_ij = P_ij (dP_ij - D_i) */
+            double dp = 0.0;
+            for (long c = 0; c < d; ++c) dp += go[c] * v[j * d + c];
+            const double ds = p[j] * (dp - Di);
+            for (long c = 0; c < d; ++c) {
+                dq[i * d + c] += scale * ds * k[j * d + c];
+                dk[j * d + c] += scale * ds * q[i * d + c];
+            }
+        }
+    }
+    free(P);
+    free(orow);
+    return FAO_OK;
+}

@@ -328,3 +328,60 @@ def test_causal_library_and_closed_forms():
     # a subset of rows with their absolute indices gives the same rows
     o3, _ = oracle.attention(q[:, :, [2, 7]], k, v, 0.3, causal=True, rows=[2, 7], nq_total=10)
     assert np.array_equal(o3, o[:, :, [2, 7]])
+
+
+def test_backward_finite_differences():
+    """dQ, dK, dV against central differences of the loss L = sum(dO * O) in float64 (the oracle's
+    forward): checks every gradient without using its formulas."""
+    rng = np.random.default_rng(16)
+    nq, nk, d, sc = 4, 6, 3, 0.7
+    q, k, v, g = _rand(rng, nq, d), _rand(rng, nk, d), _rand(rng, nk, d), _rand(rng, nq, d)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, sc)
+
+    def loss(qq, kk, vv):
+        return float((oracle.attention(qq, kk, vv, sc)[0] * g).sum())
+
+    h = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.empty_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            lp = loss(*(xp if n == name else args[n] for n in ("q", "k", "v")))
+            lm = loss(*(xm if n == name else args[n] for n in ("q", "k", "v")))
+            num[idx] = (lp - lm) / (2 * h)
+        assert np.abs(num - grad).max() <= 1e-8, name
+
+
+def test_backward_autograd_library():
+    """torch float64 autograd through SDPA on rectangular shapes (Nq != Nk != d)."""
+    rng = np.random.default_rng(17)
+    q, k, v, g = _rand(rng, 2, 3, 7, 5), _rand(rng, 2, 3, 11, 5), _rand(rng, 2, 3, 11, 5), _rand(rng, 2, 3, 7, 5)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, 0.45)
+    t = [torch.tensor(x, requires_grad=True) for x in (q, k, v)]
+    out = torch.nn.functional.scaled_dot_product_attention(*t, scale=0.45)
+    out.backward(torch.tensor(g))
+    for mine, ref in zip((dq, dk, dv), t):
+        assert np.abs(mine - ref.grad.numpy()).max() <= 1e-13
+
+
+def test_backward_page_dv_setup():
+    """[T2] Exercise 5 set-up (seed 42, N=64, d=32, blocks of 16): dV recomputed block by block from the
+    saved row max m and sum l, P_ij = exp(S_ij - m_i) / l_i, dV_j += P_ij^T dO_i, equals the oracle's dV."""
+    torch.manual_seed(42)
+    N, d, B = 64, 32, 16
+    Q, K, V = (torch.randn(N, d).double() for _ in range(3))
+    S = Q @ K.T / math.sqrt(d)
+    dO = torch.randn(N, d).double()
+    m = S.max(dim=-1, keepdim=True).values
+    l = torch.exp(S - m).sum(dim=-1, keepdim=True)
+    dV = torch.zeros(N, d, dtype=torch.float64)
+    for j in range(0, N, B):
+        for i in range(0, N, B):
+            s_ij = Q[i:i + B] @ K[j:j + B].T / math.sqrt(d)
+            p_ij = torch.exp(s_ij - m[i:i + B]) / l[i:i + B]
+            dV[j:j + B] += p_ij.T @ dO[i:i + B]
+    _, _, dv = oracle.attention_bwd(Q.numpy(), K.numpy(), V.numpy(), dO.numpy(), 1 / math.sqrt(d))
+    assert np.abs(dv - dV.numpy()).max() <= 1e-13
