@@ -134,24 +134,37 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded)}
 
 
-def traffic_record():
-    """Per-launch DRAM bytes from the committed ncu summary, if it matches the current kernel sources."""
+KERNEL_SOURCES = {
+    "mh_prefill": ("sm103_ptx.cuh", "fa_fwd_kernel.cuh", "fa_fwd_bf16.cu"),
+    "peaked_d128": ("sm103_ptx.cuh", "fa_fwd_kernel.cuh", "fa_fwd_bf16.cu"),
+    "decode": ("sm103_ptx.cuh", "fa_decode.cu"),
+}
+
+
+def sources_sha256(names):
+    """sha256 over the named kernel sources, in the given order."""
     import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_05_gb300", "csrc")
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_record():
+    """Per-launch DRAM bytes from the committed ncu summary, for each kernel whose sources are unchanged since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return {}
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "attention_forward_05_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
-    if rec.get("csrc_sha256") != h.hexdigest():
-        return {}
-    return rec.get("kernels", {})
+    out = {}
+    for key, ent in rec.get("kernels", {}).items():
+        if isinstance(ent, dict) and key in KERNEL_SOURCES and ent.get("sha256") == sources_sha256(KERNEL_SOURCES[key]):
+            out[key] = ent.get("bytes")
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm
