@@ -13,6 +13,8 @@ Entry points (same names as the C ABI):
   fa_decode_splitkv(q, k, v, splits, o=None) -> o
   fa_decode_splitkv_ex(q, k, v, splits, scale=None, workspace=None, merge_order=None, with_lse=False)
   fa_decode_workspace_bytes(B, H, d, splits)
+  fa_bwd(q, k, v, o, dout, lse, scale=None, causal=False, workspace=None) -> (dq, dk, dv)
+  fa_bwd_workspace_bytes(B, H, Nq, d)
   fa_check_device_error()
 """
 from __future__ import annotations
@@ -67,6 +69,10 @@ def lib() -> ctypes.CDLL:
             L.fa_decode_splitkv_ex.restype = i
             L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
             L.fa_decode_workspace_bytes.restype = sz
+            L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+            L.fa_bwd.restype = i
+            L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+            L.fa_bwd_workspace_bytes.restype = sz
             L.fa_check_device_error.argtypes = []
             L.fa_check_device_error.restype = i
             L.fa_status_string.argtypes = [i]
@@ -158,6 +164,52 @@ def fa_fwd_workspace_bytes(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int, d
                            causal: bool = False, kv_splits: int = 0) -> int:
     code = FA_BF16 if dtype == torch.bfloat16 else FA_FP32
     return int(lib().fa_fwd_workspace_bytes(B, H, Hkv, Nq, Nk, d, code, int(bool(causal)), int(kv_splits)))
+
+
+def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,
+           lse: torch.Tensor, scale: float | None = None, causal: bool = False,
+           dq: torch.Tensor | None = None, dk: torch.Tensor | None = None, dv: torch.Tensor | None = None,
+           workspace: torch.Tensor | None = None, stream=None):
+    """Gradients (dq, dk, dv) of attention given the forward's o and lse and the output gradient dout.
+
+    q, o, dout [B, H, Nq, d] bf16; k, v [B, Hkv, Nk, d] bf16; lse [B, H, Nq] fp32 from fa_fwd.
+    """
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("lse", lse)):
+        _need_cuda_contig(n, t)
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d], k/v [B,Hkv,Nk,d] expected")
+    if o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("o and dout must match q")
+    if q.shape[1] % k.shape[1] != 0:
+        raise ValueError("query heads must be a multiple of key/value heads")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise TypeError("q, k, v, o, dout must share a dtype")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32:
+        raise ValueError("lse must be fp32 [B,H,Nq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for n, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _need_cuda_contig(n, t)
+        if t.shape != ref.shape or t.dtype != ref.dtype:
+            raise ValueError(f"{n} must match its input")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need_cuda_contig("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, Nq, Nk, d, float(scale),
+                      _dtype_code(q), int(bool(causal)), ws_ptr, ws_bytes, _stream_handle(stream))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, Nq: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, Nq, d))
 
 
 def _decode_shapes(q, k, v):

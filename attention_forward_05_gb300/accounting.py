@@ -21,6 +21,19 @@ def fwd_flops_causal(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
     return 4 * B * H * visible * d
 
 
+def bwd_flops(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    """FLOPs of the backward's five contractions, S = Q K^T (recomputed), dP = dO V^T, dV = P^T dO,
+    dQ = dS K and dK = dS^T Q: 5 * 2 * B*H*Nq*Nk*d (2.5x the forward).  The library recomputes S
+    and dP once more for dQ; that extra work is not counted."""
+    return 10 * B * H * Nq * Nk * d
+
+
+def bwd_flops_causal(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    """bwd_flops over the (query, key) pairs a bottom-right causal mask leaves visible."""
+    visible = Nq * (Nk - Nq) + Nq * (Nq + 1) // 2
+    return 10 * B * H * visible * d
+
+
 def fwd_min_bytes(B: int, H: int, Nq: int, Nk: int, d: int, dtype: str) -> int:
     """Smallest HBM traffic of one forward: read Q, K, V once, write O and the fp32 LSE."""
     e = ESIZE[dtype]

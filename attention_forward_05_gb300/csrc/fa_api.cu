@@ -294,6 +294,103 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fa_fwd_ex(q, k, v, o, lse, B, H, H, Nq, Nk, d, scale, dtype, 0, 0, nullptr, 0, stream);
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
+  const long long align = fa::bwd_geometry(d).nq_align;
+  const long long nq_pad = (Nq + align - 1) / align * align;
+  return 2 * round256(static_cast<size_t>(B) * H * nq_pad * sizeof(float));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
+           void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int dtype, int causal,
+           void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_INVALID_ARG;
+  if (workspace && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_BF16) return FA_ERR_UNSUPPORTED;  // fp32 gradients are not built
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+  if (BH * static_cast<long long>(Nq > Nk ? Nq : Nk) * d > kMaxElems) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_bwd_workspace_bytes(B, H, Nq, d);
+  if (workspace && workspace_bytes < need) return FA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  int* err = nullptr;
+  int rc = device_setup(&dev, &err);
+  if (rc != FA_OK) return rc;
+  const fa::BwdGeometry geo = fa::bwd_geometry(d);
+  const int nq_pad = (Nq + geo.nq_align - 1) / geo.nq_align * geo.nq_align;
+  const int BHi = B * H, BHkv = B * Hkv;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  bool own_ws = false;
+  if (ws == nullptr) {
+    void* wp = nullptr;
+    cudaError_t ea = cudaMallocAsync(&wp, need, st);
+    if (ea != cudaSuccess) return cuda_fail(ea);
+    ws = static_cast<char*>(wp);
+    own_ws = true;
+  }
+  auto fail = [&](cudaError_t e) {
+    if (own_ws) cudaFreeAsync(ws, st);
+    return e != cudaSuccess ? cuda_fail(e) : FA_ERR_CUDA;
+  };
+  CUtensorMap kk, vk, qk, dok, qq, doq, kq, vq;
+  if (encode_map(&kk, k, true, BHkv, Nk, d, 64, geo.kv_keys) != FA_OK ||
+      encode_map(&vk, v, true, BHkv, Nk, d, 64, geo.kv_keys) != FA_OK ||
+      encode_map(&qk, q, true, BHi, Nq, d, 64, geo.kv_qrows) != FA_OK ||
+      encode_map(&dok, dout, true, BHi, Nq, d, 64, geo.kv_qrows) != FA_OK ||
+      encode_map(&qq, q, true, BHi, Nq, d, 64, geo.q_rows) != FA_OK ||
+      encode_map(&doq, dout, true, BHi, Nq, d, 64, geo.q_rows) != FA_OK ||
+      encode_map(&kq, k, true, BHkv, Nk, d, 64, geo.q_keys) != FA_OK ||
+      encode_map(&vq, v, true, BHkv, Nk, d, 64, geo.q_keys) != FA_OK)
+    return fail(cudaSuccess);
+  fa::BwdLaunch a;
+  a.tm_k_kv = &kk;
+  a.tm_v_kv = &vk;
+  a.tm_q_kv = &qk;
+  a.tm_do_kv = &dok;
+  a.tm_q_q = &qq;
+  a.tm_do_q = &doq;
+  a.tm_k_q = &kq;
+  a.tm_v_q = &vq;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.nl2 = reinterpret_cast<float*>(ws);
+  a.dvec = reinterpret_cast<float*>(ws + need / 2);
+  a.err = err;
+  a.BH = BHi;
+  a.BHkv = BHkv;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.Nq_pad = nq_pad;
+  a.d = d;
+  a.causal = causal;
+  a.c = scale * 1.4426950408889634f;
+  a.scale = scale;
+  a.stream = st;
+  cudaError_t e = fa::launch_bwd_bf16(a);
+  if (own_ws) {
+    cudaError_t e2 = cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 size_t fa_decode_workspace_bytes(int B, int H, int d, int splits) {
   if (B < 1 || H < 1 || splits < 1 || (d != 64 && d != 128)) return 0;
   const size_t n = static_cast<size_t>(B) * H * splits;

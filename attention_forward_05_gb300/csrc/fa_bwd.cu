@@ -1,0 +1,149 @@
+// fa_bwd.cu -- backward launches: the per-row prep pass and the bf16 instantiations of the dK/dV
+// and dQ kernels (fa_bwd_kernel.cuh).
+//
+// Source: "Flash Attention 代码填空 (Level 2-3)", Exercise 5 (recompute P from the saved row
+// statistics, dV_j += P_ij^T dO_i); the remaining gradients are the chain rule through the softmax.
+#include "fa_bwd_kernel.cuh"
+
+namespace fa {
+
+// Tile choices.  dK/dV: 128 keys per CTA, 64 query rows per step, ring depth by head size.
+// dQ: two 128-row query tiles per CTA, 64 keys per step.
+using BwdKV64 = BwdKVCfg<64, 64, 4>;
+using BwdKV128 = BwdKVCfg<128, 64, 3>;
+using BwdQ64 = BwdQCfg<64, 64, 4>;
+using BwdQ128 = BwdQCfg<128, 64, 2>;
+
+// D_i = sum_c dO_ic O_ic (fp32 over the bf16 inputs) and nl2_i = -L_i log2(e), for the rows of
+// [BH][Nq_pad]; rows i >= Nq get D = 0 and nl2 = -inf, so their P is exactly 0.
+// A group of D/8 lanes covers one row with 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                          const uint16_t* __restrict__ dout,
+                                                          const float* __restrict__ lse, float* __restrict__ nl2,
+                                                          float* __restrict__ dvec, long long rows_pad, int Nq,
+                                                          int Nq_pad) {
+  constexpr int LPR = D / 8;  // lanes per row
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long r = gt / LPR;
+  const int part = static_cast<int>(gt % LPR);
+  const bool live = r < rows_pad;
+  const long long bh = live ? r / Nq_pad : 0;
+  const int i = live ? static_cast<int>(r % Nq_pad) : 0;
+  const bool in_range = live && i < Nq;
+  float acc = 0.f;
+  if (in_range) {
+    const size_t off = (static_cast<size_t>(bh) * Nq + i) * D + part * 8;
+    const uint4 a = ldg_stream(o + off);
+    const uint4 g = ldg_stream(dout + off);
+    acc = bf16lo(a.x) * bf16lo(g.x) + bf16hi(a.x) * bf16hi(g.x);
+    acc += bf16lo(a.y) * bf16lo(g.y) + bf16hi(a.y) * bf16hi(g.y);
+    acc += bf16lo(a.z) * bf16lo(g.z) + bf16hi(a.z) * bf16hi(g.z);
+    acc += bf16lo(a.w) * bf16lo(g.w) + bf16hi(a.w) * bf16hi(g.w);
+  }
+#pragma unroll
+  for (int m = LPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (live && part == 0) {
+    dvec[r] = in_range ? acc : 0.f;
+    nl2[r] = in_range ? -lse[static_cast<size_t>(bh) * Nq + i] * 1.4426950408889634f : -INFINITY;
+  }
+}
+
+cudaError_t launch_bwd_prep(const BwdLaunch& a) {
+  const long long rows = static_cast<long long>(a.BH) * a.Nq_pad;
+  const long long threads = rows * (a.d / 8);
+  const long long blocks = (threads + 255) / 256;
+  if (blocks <= 0 || blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  if (a.d == 64)
+    fa_bwd_prep_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.nl2, a.dvec, rows, a.Nq,
+        a.Nq_pad);
+  else
+    fa_bwd_prep_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.nl2, a.dvec, rows, a.Nq,
+        a.Nq_pad);
+  return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_dkdv(const BwdLaunch& a) {
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  BwdKVParams p;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.nl2 = a.nl2;
+  p.dvec = a.dvec;
+  p.err = a.err;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.Nq_pad = a.Nq_pad;
+  p.n_kblk = (a.Nk + C::BK - 1) / C::BK;
+  p.n_qt = (a.Nq + C::BQ - 1) / C::BQ;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.causal = a.causal;
+  p.causal_off = a.Nk - a.Nq;
+  p.c = a.c;
+  p.scale = a.scale;
+  if (p.n_qt * C::BQ > a.Nq_pad) return cudaErrorInvalidValue;  // the vectors are read in whole steps
+  const long long grid = static_cast<long long>(p.n_kblk) * a.BHkv;
+  if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  fa_bwd_dkdv_kernel<C><<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream>>>(
+      *a.tm_k_kv, *a.tm_v_kv, *a.tm_q_kv, *a.tm_do_kv, p);
+  return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_dq(const BwdLaunch& a) {
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  BwdQParams p;
+  p.dq = a.dq;
+  p.nl2 = a.nl2;
+  p.dvec = a.dvec;
+  p.err = a.err;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.Nq_pad = a.Nq_pad;
+  p.n_qblk = (a.Nq + C::BR * C::NQT - 1) / (C::BR * C::NQT);
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.causal = a.causal;
+  p.causal_off = a.Nk - a.Nq;
+  p.c = a.c;
+  p.scale = a.scale;
+  const long long grid = static_cast<long long>(p.n_qblk) * a.BH;
+  if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  fa_bwd_dq_kernel<C><<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream>>>(
+      *a.tm_q_q, *a.tm_do_q, *a.tm_k_q, *a.tm_v_q, p);
+  return cudaGetLastError();
+}
+
+BwdGeometry bwd_geometry(int d) {
+  BwdGeometry g;
+  g.kv_keys = BwdKV64::BK;
+  g.kv_qrows = BwdKV64::BQ;
+  g.q_rows = BwdQ64::BR;
+  g.q_keys = BwdQ64::BC;
+  g.nq_align = BwdKV64::BQ;
+  static_assert(BwdKV64::BQ == BwdKV128::BQ && BwdQ64::BC == BwdQ128::BC, "one geometry for both head sizes");
+  (void)d;
+  return g;
+}
+
+cudaError_t launch_bwd_bf16(const BwdLaunch& a) {
+  if (a.causal && a.Nq > a.Nk) return cudaErrorInvalidValue;
+  cudaError_t e = launch_bwd_prep(a);
+  if (e != cudaSuccess) return e;
+  if (a.d == 64) {
+    if ((e = launch_dkdv<BwdKV64>(a)) != cudaSuccess) return e;
+    return launch_dq<BwdQ64>(a);
+  }
+  if ((e = launch_dkdv<BwdKV128>(a)) != cudaSuccess) return e;
+  return launch_dq<BwdQ128>(a);
+}
+
+}  // namespace fa

@@ -1,0 +1,723 @@
+// fa_bwd_kernel.cuh -- FlashAttention backward for sm_103a (bf16 operands, fp32 accumulation).
+//
+// Sources (web pages, cited by title and section):
+//   [T2] "Flash Attention 代码填空 (Level 2-3)" (boots-coder.github.io), Exercise 5: the forward keeps
+//        only O and the row statistics; the backward recomputes S_ij = Q_i K_j^T / sqrt(d) and
+//        P_ij = exp(S_ij - m_i) / l_i block by block and accumulates dV_j += P_ij^T dO_i.
+//   [T3] "CS349E 第 11 讲 01_online_softmax.py" (semidirectx.com), demo 3 remarks: the backward needs a
+//        single statistic per row, the logsumexp L = m + ln l, so that P_ij = exp(S_ij - L_i).
+// The other gradients follow from the chain rule through the row softmax:
+//   dP = dO V^T,  dS_ij = P_ij (dP_ij - D_i) with D_i = sum_c dO_ic O_ic,
+//   dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Three launches, no atomics (the result does not depend on scheduling):
+//   fa_bwd_prep_kernel  D_i and -L_i log2(e) for every query row (padded rows get 0 and -inf).
+//   fa_bwd_dkdv_kernel  one CTA per (key/value head, 128-key tile); it walks every query tile of every
+//                       query head that shares the key/value head, with S^T and dP^T computed key-major
+//                       (keys on the TMEM lanes), so P^T and dS^T are the tensor-memory A operands of
+//                       dV += P^T dO and dK += dS^T Q.  dV and dK stay in tensor memory throughout.
+//   fa_bwd_dq_kernel    one CTA per two 128-row query tiles; it walks the key tiles, recomputes S and
+//                       dP, and accumulates dQ += dS K with dS read from tensor memory.
+// Both main kernels keep the forward's warp roles: one TMA warp, one MMA-issuing warp, and two
+// warpgroups of thread-per-row elementwise work that alternate so the tensor core is never idle
+// waiting for one of them.
+#pragma once
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <int NWARPS, int MINB>
+struct RegBudget {  // registers per thread: 16384 per SM sub-partition, shared by ceil(warps/4) warps
+  static constexpr int PER_SUB = (NWARPS * MINB + 3) / 4;
+  static constexpr int RAW = (16384 / (PER_SUB * 32)) / 8 * 8;
+  static constexpr int VALUE = RAW > 248 ? 248 : RAW;
+};
+
+// wait sites recorded with a timeout (distinct from the forward's)
+enum : int { WB_KV = 0x21, WB_SF, WB_SE, WB_PF, WB_DONE, WB_Q, WB_KF, WB_VF, WB_KE, WB_VE, WB_OD, WB_DRAIN };
+
+// ------------------------------------------------------------------------------------------ dK, dV
+
+template <int D_, int BQ_, int STAGES_>
+struct BwdKVCfg {
+  static constexpr int D = D_;
+  static constexpr int BK = 128;             // keys per CTA (TMEM lanes, M of every MMA)
+  static constexpr int BQ = BQ_;             // query rows per step (N of S^T and dP^T, K of dV and dK)
+  static constexpr int STAGES = STAGES_;     // ring of (Q_i, dO_i, -L_i log2 e, D_i)
+  static constexpr int CHUNK = 64;           // bf16 elements per 128-byte swizzled row segment
+  static constexpr int NCH = D / CHUNK;
+  static constexpr int MMA_K = 16;
+  static constexpr int KV_CH_BYTES = BK * 128;
+  static constexpr int KV_BYTES = NCH * KV_CH_BYTES;
+  static constexpr int QS_CH_BYTES = BQ * 128;
+  static constexpr int QS_BYTES = NCH * QS_CH_BYTES;
+  static constexpr int VEC_BYTES = BQ * 4;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;              // stage s at + s * QS_BYTES
+  static constexpr int OFF_DO = OFF_Q + STAGES * QS_BYTES;
+  static constexpr int OFF_VEC = OFF_DO + STAGES * QS_BYTES;  // stage s: nl2 at + 2 s VEC, D at + (2 s + 1) VEC
+  static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * VEC_BYTES;
+  // barriers: kv_full, st_full[S], st_empty[S], s_full[2], p_full[2], done, drain
+  static constexpr int NBAR = 1 + 2 * STAGES + 4 + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // TMEM: slot b (b = 0, 1) holds S^T at b*2*BQ and dP^T at b*2*BQ + BQ; P^T and dS^T (bf16 pairs)
+  // are written over the first BQ/2 columns of each.  dV and dK accumulate after the slots.
+  static constexpr int COL_DV = 4 * BQ;
+  static constexpr int COL_DK = 4 * BQ + D;
+  static constexpr int TMEM_NEED = 4 * BQ + 2 * D;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int NWARPS = 10;
+  static constexpr int NTHREADS = NWARPS * 32;
+  static constexpr int LOAD_WARP = 8;
+  static constexpr int MMA_WARP = 9;
+  static constexpr int MAXREG = RegBudget<NWARPS, 1>::VALUE;
+  static_assert(D % CHUNK == 0 && BQ % 32 == 0 && BQ <= 128, "tile");
+  static_assert(TMEM_NEED <= 512, "tensor memory");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(QS_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+};
+
+struct BwdKVParams {
+  void* dk;              // [B, Hkv, Nk, D] bf16
+  void* dv;
+  const float* nl2;      // [B*H][Nq_pad]: -L_i log2(e), -inf for padded rows
+  const float* dvec;     // [B*H][Nq_pad]: D_i, 0 for padded rows
+  int* err;
+  int Nq, Nk, Nq_pad, n_kblk, n_qt;
+  int H, Hkv;
+  int causal, causal_off;  // query row i sees keys j <= i + causal_off
+  float c;                 // scale * log2(e)
+  float scale;
+};
+
+template <class C>
+__global__ void __maxnreg__(C::MAXREG)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdKVParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int kb = static_cast<int>(blockIdx.x % p.n_kblk);  // low key tiles first: with a causal mask they see most rows
+  const int kvbh = static_cast<int>(blockIdx.x / p.n_kblk);
+  const int b = kvbh / p.Hkv;
+  const int g = kvbh % p.Hkv;
+  const int G = p.H / p.Hkv;  // query heads per key/value head
+  const int k0 = kb * C::BK;
+  // query tiles that see at least one key of the tile: rows i >= k0 - causal_off
+  const int i_lo = p.causal ? max(0, k0 - p.causal_off) / C::BQ : 0;
+  const int per_head = p.n_qt - i_lo;
+  const int T = G * per_head;  // steps: (query head, query tile) pairs, >= 1
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t bar_kv = bar0;
+  auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_empty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
+  auto bar_sf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + w); };
+  auto bar_pf = [&](int w) { return bar0 + 8u * (3 + 2 * C::STAGES + w); };
+  const uint32_t bar_done = bar0 + 8u * (5 + 2 * C::STAGES);
+  const uint32_t bar_drain = bar0 + 8u * (6 + 2 * C::STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bar_sf(w), 1);
+      mbar_init(bar_pf(w), 4);  // one arrive per warp of the warpgroup
+    }
+    mbar_init(bar_done, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::LOAD_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto step_head = [&](int s) { return b * p.H + g * G + s / per_head; };  // query (batch, head) index
+  auto step_qt = [&](int s) { return i_lo + s % per_head; };               // query tile
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int n_done = 0;
+      mbar_expect_tx(bar_kv, 2 * C::KV_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c) {
+        tma_load_3d(sbase + C::OFF_K + c * C::KV_CH_BYTES, &tm_k, bar_kv, c * C::CHUNK, k0, kvbh);
+        tma_load_3d(sbase + C::OFF_V + c * C::KV_CH_BYTES, &tm_v, bar_kv, c * C::CHUNK, k0, kvbh);
+      }
+      for (int s = 0; s < T; ++s) {
+        const int st = s % C::STAGES;
+        if (!mbar_wait(bar_empty(st), ((s / C::STAGES) & 1) ^ 1, abort_flag, p.err, WB_SE)) break;
+        const int bh = step_head(s);
+        const int q0 = step_qt(s) * C::BQ;
+        mbar_expect_tx(bar_full(st), 2 * C::QS_BYTES + 2 * C::VEC_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_3d(sbase + C::OFF_Q + st * C::QS_BYTES + c * C::QS_CH_BYTES, &tm_q, bar_full(st), c * C::CHUNK,
+                      q0, bh);
+          tma_load_3d(sbase + C::OFF_DO + st * C::QS_BYTES + c * C::QS_CH_BYTES, &tm_do, bar_full(st),
+                      c * C::CHUNK, q0, bh);
+        }
+        const size_t vo = static_cast<size_t>(bh) * p.Nq_pad + q0;
+        bulk_load_1d(sbase + C::OFF_VEC + st * 2 * C::VEC_BYTES, p.nl2 + vo, C::VEC_BYTES, bar_full(st));
+        bulk_load_1d(sbase + C::OFF_VEC + (st * 2 + 1) * C::VEC_BYTES, p.dvec + vo, C::VEC_BYTES, bar_full(st));
+        n_done = s + 1;
+      }
+      // drain every copy issued above before the CTA exits
+      mbar_wait_drain(bar_kv, 0, p.err, WB_DRAIN);
+#pragma unroll
+      for (int st = 0; st < C::STAGES; ++st) {
+        const int cnt = n_done > st ? (n_done - 1 - st) / C::STAGES + 1 : 0;
+        if (cnt > 0) mbar_wait_drain(bar_full(st), (cnt - 1) & 1, p.err, WB_DRAIN);
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer (whole warp, elected issue)
+    auto wait_all = [&](uint32_t bar, uint32_t parity, int where) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where));
+    };
+    constexpr uint32_t idesc_s = make_idesc(1, C::BK, C::BQ, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
+    constexpr uint32_t idesc_g = make_idesc(1, C::BK, C::D, 0, 1);   // dV += P^T dO, dK += dS^T Q (B MN-major)
+    const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+    const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+    const uint64_t dqk0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);               // Q as K-major B
+    const uint64_t ddok0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);             // dO as K-major B
+    const uint64_t dqm0 = sdesc_sw128(sbase + C::OFF_Q, C::QS_CH_BYTES, 1024);   // Q as MN-major B
+    const uint64_t ddom0 = sdesc_sw128(sbase + C::OFF_DO, C::QS_CH_BYTES, 1024); // dO as MN-major B
+    auto issue_scores = [&](int s) {
+      const int st = s % C::STAGES;
+      const uint32_t col = (s & 1) * 2 * C::BQ;
+      const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+        const int e = kk * C::MMA_K;
+        const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        if (elect_one()) mma_ss<0>(tmem + col, dk0 + oa, dqk0 + so + ob, idesc_s, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+        const int e = kk * C::MMA_K;
+        const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        if (elect_one()) mma_ss<0>(tmem + col + C::BQ, dv0 + oa, ddok0 + so + ob, idesc_s, kk > 0);
+      }
+    };
+    auto issue_grads = [&](int s) {
+      const int st = s % C::STAGES;
+      const uint32_t col = (s & 1) * 2 * C::BQ;
+      const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+        const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
+        if (elect_one())
+          mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
+                    (s > 0 || kk > 0) ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+        const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+        if (elect_one())
+          mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
+                    (s > 0 || kk > 0) ? 1u : 0u);
+      }
+    };
+    auto commit = [&](uint32_t bar) {
+      if (elect_one()) mma_commit(bar);
+      __syncwarp();
+    };
+    bool ok = wait_all(bar_kv, 0, WB_KV);
+    for (int s = 0; ok && s <= T; ++s) {
+      if (s < T) {
+        // slot s & 1 was last read by the gradient MMAs of step s - 2, issued before this point
+        ok = wait_all(bar_full(s % C::STAGES), (s / C::STAGES) & 1, WB_SF);
+        if (!ok) break;
+        tc_fence_after();
+        issue_scores(s);
+        commit(bar_sf(s & 1));
+      }
+      if (s > 0) {
+        const int r = s - 1;
+        ok = wait_all(bar_pf(r & 1), (r >> 1) & 1, WB_PF);
+        if (!ok) break;
+        tc_fence_after();
+        issue_grads(r);
+        commit(bar_empty(r % C::STAGES));
+      }
+    }
+    if (ok) commit(bar_done);
+    commit(bar_drain);
+    mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
+  } else {
+    // ------------------------------------------------------------ elementwise warpgroups
+    // Warpgroup w handles the steps s with s % 2 == w; thread = key row (TMEM lane).
+    const int w = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int key = k0 + row;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + w * 2 * C::BQ;
+    const uint32_t tdP = tS + C::BQ;
+    const uint64_t c2 = f2_pack(p.c, p.c);
+    bool ok = true;
+    for (int s = w; s < T; s += 2) {
+      const int st = s % C::STAGES;
+      bool okw = mbar_wait(bar_sf(w), (s >> 1) & 1, abort_flag, p.err, WB_SF);
+      // the stage's vectors came by TMA: observe its completion (already complete) before reading them
+      okw = okw && mbar_wait(bar_full(st), (s / C::STAGES) & 1, abort_flag, p.err, WB_SF);
+      ok = __all_sync(0xffffffffu, okw);
+      if (!ok) break;
+      tc_fence_after();
+      const float* nl2 = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 2 * C::VEC_BYTES);
+      const float* dv = reinterpret_cast<const float*>(smem + C::OFF_VEC + (st * 2 + 1) * C::VEC_BYTES);
+      // causal: query column q (row step_qt(s)*BQ + q) is visible to this key when q >= qmin
+      const int qmin = p.causal ? key - p.causal_off - step_qt(s) * C::BQ : -1;
+      uint32_t pk_p[C::BQ / 64][32], pk_ds[C::BQ / 64][32];
+#pragma unroll
+      for (int cc = 0; cc < C::BQ / 32; ++cc) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + cc * 32, sr);
+        tmem_ld32(tdP + cc * 32, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int q = cc * 32 + e;
+          const float2 nl = *reinterpret_cast<const float2*>(nl2 + q);
+          const float2 dd = *reinterpret_cast<const float2*>(dv + q);
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+                                    f2_pack(nl.x, nl.y));
+          float x0, x1;
+          f2_unpack_f(x, x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (q < qmin) p0 = 0.f;
+          if (q + 1 < qmin) p1 = 0.f;
+          const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                    f2_pack(-dd.x, -dd.y));
+          const uint64_t ds = f2_mul(f2_pack(p0, p1), t);
+          float ds0, ds1;
+          f2_unpack_f(ds, ds0, ds1);
+          const int word = q / 2;
+          pk_p[word / 32][word % 32] = pack_bf16x2(p0, p1);
+          pk_ds[word / 32][word % 32] = pack_bf16x2(ds0, ds1);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < C::BQ / 64; ++i) {
+        tmem_st32(tS + i * 32, pk_p[i]);
+        tmem_st32(tdP + i * 32, pk_ds[i]);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pf(w));
+    }
+    // ---------------------------------------------------------- epilogue: warpgroup 0 writes dV, 1 writes dK
+    bool okd = ok && mbar_wait(bar_done, 0, abort_flag, p.err, WB_DONE);
+    okd = __all_sync(0xffffffffu, okd);
+    if (okd) {
+      tc_fence_after();
+      const float mul = w == 0 ? 1.f : p.scale;
+      const uint32_t tacc = tmem + lane_base + (w == 0 ? C::COL_DV : C::COL_DK);
+      uint8_t* out = static_cast<uint8_t*>(w == 0 ? p.dv : p.dk) +
+                     (static_cast<size_t>(kvbh) * p.Nk + key) * (C::D * 2);
+      const bool in_range = key < p.Nk;
+#pragma unroll
+      for (int cc = 0; cc < C::D / 32; ++cc) {
+        uint32_t a[32];
+        tmem_ld32(tacc + cc * 32, a);
+        tmem_wait_ld();
+        reg_fence(a);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(out + cc * 64);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 wv;
+            wv.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * mul, __uint_as_float(a[8 * v4 + 1]) * mul);
+            wv.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * mul, __uint_as_float(a[8 * v4 + 3]) * mul);
+            wv.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * mul, __uint_as_float(a[8 * v4 + 5]) * mul);
+            wv.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * mul, __uint_as_float(a[8 * v4 + 7]) * mul);
+            dst[v4] = wv;
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::LOAD_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------------ dQ
+
+template <int D_, int BC_, int STAGES_>
+struct BwdQCfg {
+  static constexpr int D = D_;
+  static constexpr int BR = 128;           // query rows per tile (TMEM lanes)
+  static constexpr int NQT = 2;            // query tiles per CTA, alternating between the two warpgroups
+  static constexpr int BC = BC_;           // keys per step
+  static constexpr int STAGES = STAGES_;   // ring of (K_j, V_j)
+  static constexpr int CHUNK = 64;
+  static constexpr int NCH = D / CHUNK;
+  static constexpr int MMA_K = 16;
+  static constexpr int Q_CH_BYTES = BR * 128;
+  static constexpr int Q_BYTES = NCH * Q_CH_BYTES;
+  static constexpr int KV_CH_BYTES = BC * 128;
+  static constexpr int KV_BYTES = NCH * KV_CH_BYTES;
+  static constexpr int OFF_Q = 0;                              // tile t at + t * Q_BYTES
+  static constexpr int OFF_DO = OFF_Q + NQT * Q_BYTES;
+  static constexpr int OFF_K = OFF_DO + NQT * Q_BYTES;         // stage s at + s * KV_BYTES
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT], drain
+  static constexpr int NBAR = 1 + 4 * STAGES + 3 * NQT + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // TMEM: tile t holds S at t*2*BC and dP at t*2*BC + BC (dS, bf16 pairs, over the first BC/2 columns
+  // of S), dQ at 2*NQT*BC + t*D.
+  static constexpr int COL_DQ = 2 * NQT * BC;
+  static constexpr int TMEM_NEED = 2 * NQT * BC + NQT * D;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int NWARPS = 4 * NQT + 2;
+  static constexpr int NTHREADS = NWARPS * 32;
+  static constexpr int LOAD_WARP = 4 * NQT;
+  static constexpr int MMA_WARP = 4 * NQT + 1;
+  static constexpr int MAXREG = RegBudget<NWARPS, 1>::VALUE;
+  static_assert(D % CHUNK == 0 && BC % 64 == 0 && BC <= 128, "tile");
+  static_assert(TMEM_NEED <= 512, "tensor memory");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+struct BwdQParams {
+  void* dq;              // [B, H, Nq, D] bf16
+  const float* nl2;      // [B*H][Nq_pad]
+  const float* dvec;     // [B*H][Nq_pad]
+  int* err;
+  int Nq, Nk, Nq_pad, n_qblk;
+  int H, Hkv;
+  int causal, causal_off;
+  float c, scale;
+};
+
+template <class C>
+__global__ void __maxnreg__(C::MAXREG)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const BwdQParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // with a causal mask the query blocks run last-to-first, so the longest CTAs start first
+  const int qb = p.causal ? p.n_qblk - 1 - static_cast<int>(blockIdx.x % p.n_qblk)
+                          : static_cast<int>(blockIdx.x % p.n_qblk);
+  const int bh = static_cast<int>(blockIdx.x / p.n_qblk);
+  const int kvh = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);
+  const int q0 = qb * C::BR * C::NQT;
+  const int k_hi = p.causal ? min(p.Nk, q0 + C::NQT * C::BR + p.causal_off) : p.Nk;
+  const int T = (k_hi + C::BC - 1) / C::BC;  // >= 1: every row sees at least one key
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t bar_q = bar0;
+  auto bar_kf = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_vf = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
+  auto bar_ke = [&](int s) { return bar0 + 8u * (1 + 2 * C::STAGES + s); };
+  auto bar_ve = [&](int s) { return bar0 + 8u * (1 + 3 * C::STAGES + s); };
+  auto bar_sf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + t); };
+  auto bar_pf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + C::NQT + t); };
+  auto bar_od = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 2 * C::NQT + t); };
+  const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_kf(s), 1);
+      mbar_init(bar_vf(s), 1);
+      mbar_init(bar_ke(s), 1);
+      mbar_init(bar_ve(s), 1);
+    }
+    for (int t = 0; t < C::NQT; ++t) {
+      mbar_init(bar_sf(t), 1);
+      mbar_init(bar_pf(t), 4);
+      mbar_init(bar_od(t), 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::LOAD_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::LOAD_WARP) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int nk_done = 0, nv_done = 0;
+      mbar_expect_tx(bar_q, 2 * C::NQT * C::Q_BYTES);
+#pragma unroll
+      for (int t = 0; t < C::NQT; ++t)
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_3d(sbase + C::OFF_Q + t * C::Q_BYTES + c * C::Q_CH_BYTES, &tm_q, bar_q, c * C::CHUNK,
+                      q0 + t * C::BR, bh);
+          tma_load_3d(sbase + C::OFF_DO + t * C::Q_BYTES + c * C::Q_CH_BYTES, &tm_do, bar_q, c * C::CHUNK,
+                      q0 + t * C::BR, bh);
+        }
+      for (int j = 0; j < T; ++j) {
+        const int s = j % C::STAGES;
+        const uint32_t ph = ((j / C::STAGES) & 1) ^ 1;
+        if (!mbar_wait(bar_ke(s), ph, abort_flag, p.err, WB_KE)) break;
+        mbar_expect_tx(bar_kf(s), C::KV_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sbase + C::OFF_K + s * C::KV_BYTES + c * C::KV_CH_BYTES, &tm_k, bar_kf(s), c * C::CHUNK,
+                      j * C::BC, kvh);
+        nk_done = j + 1;
+        if (!mbar_wait(bar_ve(s), ph, abort_flag, p.err, WB_VE)) break;
+        mbar_expect_tx(bar_vf(s), C::KV_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sbase + C::OFF_V + s * C::KV_BYTES + c * C::KV_CH_BYTES, &tm_v, bar_vf(s), c * C::CHUNK,
+                      j * C::BC, kvh);
+        nv_done = j + 1;
+      }
+      mbar_wait_drain(bar_q, 0, p.err, WB_DRAIN);
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) {
+        const int nks = nk_done > s ? (nk_done - 1 - s) / C::STAGES + 1 : 0;
+        const int nvs = nv_done > s ? (nv_done - 1 - s) / C::STAGES + 1 : 0;
+        if (nks > 0) mbar_wait_drain(bar_kf(s), (nks - 1) & 1, p.err, WB_DRAIN);
+        if (nvs > 0) mbar_wait_drain(bar_vf(s), (nvs - 1) & 1, p.err, WB_DRAIN);
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    auto wait_all = [&](uint32_t bar, uint32_t parity, int where) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where));
+    };
+    constexpr uint32_t idesc_s = make_idesc(1, C::BR, C::BC, 0, 0);  // S = Q K^T, dP = dO V^T
+    constexpr uint32_t idesc_g = make_idesc(1, C::BR, C::D, 0, 1);   // dQ += dS K (K MN-major)
+    const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+    const uint64_t ddo0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+    const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+    const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+    const uint64_t dkm0 = sdesc_sw128(sbase + C::OFF_K, C::KV_CH_BYTES, 1024);
+    auto issue_scores = [&](int t, int s) {
+      const uint32_t col = t * 2 * C::BC;
+      const uint64_t to = static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
+      const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+        const int e = kk * C::MMA_K;
+        const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        if (elect_one()) mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+        const int e = kk * C::MMA_K;
+        const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        if (elect_one()) mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
+      }
+    };
+    auto issue_dq = [&](int t, int s, bool acc) {
+      const uint32_t a_tmem = tmem + t * 2 * C::BC;
+      const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
+        const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+        if (elect_one())
+          mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
+                    (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    auto commit = [&](uint32_t bar) {
+      if (elect_one()) mma_commit(bar);
+      __syncwarp();
+    };
+    bool ok = wait_all(bar_q, 0, WB_Q) && wait_all(bar_kf(0), 0, WB_KF) && wait_all(bar_vf(0), 0, WB_VF);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < C::NQT; ++t) {
+        issue_scores(t, 0);
+        commit(bar_sf(t));
+      }
+      commit(bar_ve(0));
+    }
+    for (int j = 0; ok && j < T; ++j) {
+      const int s = j % C::STAGES;
+      const int j1 = j + 1;
+      const int s1 = j1 % C::STAGES;
+      if (j1 < T) {
+        ok = wait_all(bar_kf(s1), (j1 / C::STAGES) & 1, WB_KF) && wait_all(bar_vf(s1), (j1 / C::STAGES) & 1, WB_VF);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int t = 0; t < C::NQT; ++t) {
+        ok = wait_all(bar_pf(t), j & 1, WB_PF);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dq(t, s, j > 0);
+        if (t == C::NQT - 1) commit(bar_ke(s));
+        if (j1 < T) {
+          issue_scores(t, s1);
+          commit(bar_sf(t));
+          if (t == C::NQT - 1) commit(bar_ve(s1));
+        } else {
+          commit(bar_od(t));
+        }
+      }
+    }
+    commit(bar_drain);
+    mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
+  } else {
+    // ------------------------------------------------------------ elementwise warpgroups: thread = query row
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int qrow = q0 + t * C::BR + row;
+    const bool in_range = qrow < p.Nq;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 2 * C::BC;
+    const uint32_t tdP = tS + C::BC;
+    const size_t vrow = static_cast<size_t>(bh) * p.Nq_pad + qrow;
+    const float nl = in_range ? p.nl2[vrow] : -INFINITY;
+    const float dd = in_range ? p.dvec[vrow] : 0.f;
+    const int row_lim = p.causal ? min(p.Nk, qrow + 1 + p.causal_off) : p.Nk;  // keys [0, row_lim) visible
+    const uint64_t c2 = f2_pack(p.c, p.c);
+    const uint64_t nl_2 = f2_pack(nl, nl);
+    const uint64_t nd_2 = f2_pack(-dd, -dd);
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, WB_SF);
+      ok = __all_sync(0xffffffffu, okw);
+      if (!ok) break;
+      tc_fence_after();
+      const int valid = row_lim - j * C::BC;
+      uint32_t pk[C::BC / 64][32];
+#pragma unroll
+      for (int cc = 0; cc < C::BC / 32; ++cc) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tS + cc * 32, sr);
+        tmem_ld32(tdP + cc * 32, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int col = cc * 32 + e;
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nl_2);
+          float x0, x1;
+          f2_unpack_f(x, x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (col >= valid) p0 = 0.f;
+          if (col + 1 >= valid) p1 = 0.f;
+          const uint64_t tt = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd_2);
+          const uint64_t ds = f2_mul(f2_pack(p0, p1), tt);
+          float ds0, ds1;
+          f2_unpack_f(ds, ds0, ds1);
+          const int word = col / 2;
+          pk[word / 32][word % 32] = pack_bf16x2(ds0, ds1);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < C::BC / 64; ++i) tmem_st32(tS + i * 32, pk[i]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pf(t));
+    }
+    bool okd = ok && mbar_wait(bar_od(t), 0, abort_flag, p.err, WB_OD);
+    okd = __all_sync(0xffffffffu, okd);
+    if (okd) {
+      tc_fence_after();
+      const uint32_t tacc = tmem + lane_base + C::COL_DQ + t * C::D;
+      uint8_t* out = static_cast<uint8_t*>(p.dq) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * 2);
+#pragma unroll
+      for (int cc = 0; cc < C::D / 32; ++cc) {
+        uint32_t a[32];
+        tmem_ld32(tacc + cc * 32, a);
+        tmem_wait_ld();
+        reg_fence(a);
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(out + cc * 64);
+          const float mul = p.scale;
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 wv;
+            wv.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * mul, __uint_as_float(a[8 * v4 + 1]) * mul);
+            wv.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * mul, __uint_as_float(a[8 * v4 + 3]) * mul);
+            wv.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * mul, __uint_as_float(a[8 * v4 + 5]) * mul);
+            wv.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * mul, __uint_as_float(a[8 * v4 + 7]) * mul);
+            dst[v4] = wv;
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::LOAD_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace fa

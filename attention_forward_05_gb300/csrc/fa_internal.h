@@ -54,6 +54,45 @@ cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a);
 cudaError_t launch_fwd_fp32_d64(const FwdLaunch& a);
 cudaError_t launch_fwd_fp32_d128(const FwdLaunch& a);
 
+struct BwdLaunch {
+  // maps for the dK/dV kernel: K, V boxes (64 cols, kv_keys rows); Q, dO boxes (64 cols, kv_qrows rows)
+  const CUtensorMap* tm_k_kv;
+  const CUtensorMap* tm_v_kv;
+  const CUtensorMap* tm_q_kv;
+  const CUtensorMap* tm_do_kv;
+  // maps for the dQ kernel: Q, dO boxes (64 cols, q_rows rows); K, V boxes (64 cols, q_keys rows)
+  const CUtensorMap* tm_q_q;
+  const CUtensorMap* tm_do_q;
+  const CUtensorMap* tm_k_q;
+  const CUtensorMap* tm_v_q;
+  const void* o;            // [BH, Nq, d] bf16 forward output
+  const void* dout;         // [BH, Nq, d] bf16
+  const float* lse;         // [BH, Nq] natural-log LSE of the forward
+  void* dq;                 // [BH, Nq, d] bf16
+  void* dk;                 // [BHkv, Nk, d] bf16
+  void* dv;
+  float* nl2;               // workspace [BH][Nq_pad]
+  float* dvec;              // workspace [BH][Nq_pad]
+  int* err;
+  int BH, BHkv, H, Hkv, Nq, Nk, Nq_pad, d;
+  int causal;
+  float c;                  // scale * log2(e)
+  float scale;
+  cudaStream_t stream;
+};
+
+struct BwdGeometry {
+  int kv_keys;   // keys per dK/dV CTA
+  int kv_qrows;  // query rows per dK/dV step
+  int q_rows;    // query rows per dQ tile
+  int q_keys;    // keys per dQ step
+  int nq_align;  // Nq_pad is Nq rounded up to this
+};
+
+BwdGeometry bwd_geometry(int d);
+// prep pass, then dK/dV, then dQ, in stream order
+cudaError_t launch_bwd_bf16(const BwdLaunch& a);
+
 struct DecodeLaunch {
   const void* q;            // [BH, d] bf16
   const void* k;            // [BH, Nk, d] bf16

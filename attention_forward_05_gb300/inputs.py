@@ -11,6 +11,7 @@ then rounded to the storage dtype with round-to-nearest-even):
   peaked_d128     B=2  H=16 Nq=Nk=8192   d=128 bf16, Q,K ~ 3 N(0,1), V ~ N(0,1)
   decode          B=32 H=32 Nq=1 Nk=32768 d=64 bf16, N(0,1), 16 splits, seeded merge order
 The decode merge order is numpy.random.default_rng(seed).permutation(splits).
+The output gradient dO of a backward pass is N(0,1), rounded to the storage dtype (make_dout).
 """
 from __future__ import annotations
 
@@ -77,6 +78,15 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, dtype="bf16", seed: int =
     k = _draw((B, H, Nk, d), gen, dev, qk_mult, tdt)
     v = _draw((B, H, Nk, d), gen, dev, v_mult, tdt)
     return q, k, v
+
+
+def make_dout(B: int, H: int, Nq: int, d: int, dtype="bf16", seed: int = 0, device="cpu") -> torch.Tensor:
+    """dO [B,H,Nq,d]: N(0,1) draws from a generator seeded with `seed`, rounded to the dtype."""
+    tdt = dtype if isinstance(dtype, torch.dtype) else (torch.float32 if dtype == "fp32" else torch.bfloat16)
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(seed))
+    return _draw((B, H, Nq, d), gen, dev, 1.0, tdt)
 
 
 def workload_inputs(w: Workload, device="cpu"):

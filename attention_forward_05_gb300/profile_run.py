@@ -2,6 +2,7 @@
 
     python -m attention_forward_05_gb300.profile_run --workload mh_prefill --launches 2
     python -m attention_forward_05_gb300.profile_run --workload decode --B 4 --launches 2
+    python -m attention_forward_05_gb300.profile_run --workload mh_prefill --bwd --launches 2
 
 The first launch is a warm-up; the process exits 0 after a device synchronise
 and a device-error check.  --B / --H override the workload's batch and heads
@@ -17,7 +18,7 @@ import torch
 
 import attention_forward_05_gb300 as fa
 from attention_forward_05_gb300 import accounting
-from attention_forward_05_gb300.inputs import WORKLOADS, merge_order, workload_inputs
+from attention_forward_05_gb300.inputs import WORKLOADS, make_dout, merge_order, workload_inputs
 
 
 def main(argv=None) -> int:
@@ -28,6 +29,7 @@ def main(argv=None) -> int:
     ap.add_argument("--H", type=int, default=0)
     ap.add_argument("--time", action="store_true", help="time the launches with CUDA events and print the rate")
     ap.add_argument("--causal", action="store_true", help="causal mask (prefill workloads)")
+    ap.add_argument("--bwd", action="store_true", help="time the backward (fa_bwd) after one forward (bf16 prefill)")
     a = ap.parse_args(argv)
     w = WORKLOADS[a.workload]
     if a.B:
@@ -40,8 +42,19 @@ def main(argv=None) -> int:
     o = torch.empty_like(q) if not w.splits else None
     lse = torch.empty((w.B, w.H, w.Nq), device=dev) if not w.splits else None
 
+    if a.bwd:
+        if w.splits or w.dtype != "bf16":
+            ap.error("--bwd takes a bf16 prefill workload")
+        dout = make_dout(w.B, w.H, w.Nq, w.d, "bf16", seed=w.seed + 700, device=dev)
+        fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse, causal=a.causal)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
+
     def run():
-        if w.splits:
+        if a.bwd:
+            fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale, causal=a.causal, dq=grads[0], dk=grads[1], dv=grads[2],
+                      workspace=ws)
+        elif w.splits:
             fa.fa_decode_splitkv_ex(q, k, v, w.splits, merge_order=order)
         else:
             fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse, causal=a.causal)
@@ -56,7 +69,11 @@ def main(argv=None) -> int:
     torch.cuda.synchronize()
     if a.time and a.launches:
         ms = start.elapsed_time(end) / a.launches
-        if w.splits:
+        if a.bwd:
+            fl = accounting.bwd_flops_causal(w.B, w.H, w.Nq, w.Nk, w.d) if a.causal else \
+                accounting.bwd_flops(w.B, w.H, w.Nq, w.Nk, w.d)
+            rate = f"{fl / ms / 1e9:.1f} TFLOP/s (backward{', causal' if a.causal else ''})"
+        elif w.splits:
             rate = f"{accounting.decode_min_bytes(w.B, w.H, w.Nk, w.d) / ms / 1e6:.1f} GB/s"
         elif a.causal:
             rate = f"{accounting.fwd_flops_causal(w.B, w.H, w.Nq, w.Nk, w.d) / ms / 1e9:.1f} TFLOP/s (causal)"

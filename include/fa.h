@@ -105,6 +105,36 @@ size_t fa_fwd_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int 
                               int causal, int kv_splits);
 
 /*
+ * fa_bwd -- gradients of exact attention (bf16 operands, fp32 accumulation).
+ * Given the forward's inputs, its output O and natural-log LSE, and dO (the
+ * gradient of a loss with respect to O), writes
+ *   dV = P^T dO, dQ = scale dS K, dK = scale dS^T Q, with P = exp(scale Q K^T - LSE)
+ *   recomputed block by block from the saved LSE ("Flash Attention 代码填空
+ *   (Level 2-3)", Exercise 5: the forward keeps O and the row statistics, the
+ *   backward rebuilds P_ij and accumulates dV_j += P_ij^T dO_i), dP = dO V^T and
+ *   dS = P * (dP - D), D_i = sum_c dO_ic O_ic (chain rule through the softmax).
+ *   q, o, dout, dq  [B, H, Nq, d] bf16       k, v, dk, dv [B, Hkv, Nk, d] bf16
+ *   lse             [B, H, Nq] fp32 in: as written by fa_fwd / fa_fwd_ex
+ *   Hkv, causal     as in fa_fwd_ex; with Hkv < H, dk and dv sum over the query
+ *                   heads that share a key/value head.
+ *   dtype           FA_BF16 only (FA_FP32 returns FA_ERR_UNSUPPORTED); d 64 or 128.
+ *   workspace       device buffer of at least fa_bwd_workspace_bytes(B, H, Nq, d)
+ *                   bytes (16-byte aligned) for D and the rescaled LSE, or NULL
+ *                   to allocate it stream-ordered on `stream`.
+ * No atomics: every gradient element is written once, by one CTA, so repeated
+ * calls give bit-identical results.  Inputs are read only; outputs are fully
+ * overwritten.  Returns FA_OK or an fa_status code; argument errors are
+ * reported before anything is launched.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv,
+           int Nq, int Nk, int d, float scale, int dtype, int causal,
+           void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Bytes of workspace fa_bwd needs (0 for invalid arguments). */
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
+
+/*
  * fa_decode_splitkv -- attention of one bf16 query per head over Nk keys,
  * split into `splits` chunks of ceil(Nk/splits) keys processed in parallel
  * (flash-decoding); each chunk yields a partial state (m, l, o) with o

@@ -76,6 +76,10 @@ def _load():
             lib.fao_attention_bwd_head.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
                                                    ctypes.c_long, ctypes.c_long, ctypes.c_double]
             lib.fao_attention_bwd_head.restype = ctypes.c_int
+            lib.fao_attention_bwd_head_limits.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
+                                                          ctypes.c_long, ctypes.c_long, ctypes.c_double,
+                                                          ctypes.POINTER(ctypes.c_long)]
+            lib.fao_attention_bwd_head_limits.restype = ctypes.c_int
             lib.fao_partial_state.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
                                               ctypes.c_double, _dp, _dp, _dp]
             lib.fao_partial_state.restype = ctypes.c_int
@@ -181,25 +185,48 @@ def _attention_causal(q, k, v, scale, rows, nq_total):
     return o.reshape(lead + (nq, d)), lse.reshape(lead + (nq,))
 
 
-def attention_bwd(q, k, v, dout, scale: float):
+def attention_bwd(q, k, v, dout, scale: float, causal: bool = False):
     """Gradients (dQ, dK, dV) of exact attention for a loss whose gradient w.r.t. O is dout.
 
-    q, dout [..., Nq, d]; k, v [..., Nk, d] with matching leading dimensions.  float64 arrays.
+    q, dout [..., H, Nq, d]; k, v [..., Hkv, Nk, d] with H a multiple of Hkv: query head h reads
+    key/value head h // (H // Hkv), and dK, dV of a shared head sum the contributions of its
+    query heads.  causal: row i sees keys 0 .. i + Nk - Nq (bottom-right aligned).
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
-    lead = q.shape[:-2]
     nq, d = q.shape[-2:]
     nk = k.shape[-2]
+    H, Hkv = (q.shape[-3], k.shape[-3]) if q.ndim >= 3 else (1, 1)
+    group = H // Hkv
+    if group > 1:
+        k, v = np.repeat(k, group, axis=-3), np.repeat(v, group, axis=-3)
+    lead = q.shape[:-2]
     qf, kf, vf, gf = q.reshape(-1, nq, d), k.reshape(-1, nk, d), v.reshape(-1, nk, d), dout.reshape(-1, nq, d)
     dq, dk, dv = np.empty_like(qf), np.empty_like(kf), np.empty_like(vf)
+    lim = None
+    if causal:
+        lim = np.ascontiguousarray(causal_limits(np.arange(nq), nq, nk), dtype=np.int64)
+        if (lim < 1).any():
+            raise ValueError("causal mask needs Nq <= Nk")
     L = _load()
     for h in range(qf.shape[0]):
         a, b, c_, g = (np.ascontiguousarray(x[h]) for x in (qf, kf, vf, gf))
         oq, ok_, ov = np.empty((nq, d)), np.empty((nk, d)), np.empty((nk, d))
-        _check(L.fao_attention_bwd_head(_ptr(a), _ptr(b), _ptr(c_), _ptr(g), _ptr(oq), _ptr(ok_), _ptr(ov), nq, nk,
-                                        d, float(scale)), "attention_bwd")
+        if lim is None:
+            rc = L.fao_attention_bwd_head(_ptr(a), _ptr(b), _ptr(c_), _ptr(g), _ptr(oq), _ptr(ok_), _ptr(ov), nq, nk,
+                                          d, float(scale))
+        else:
+            rc = L.fao_attention_bwd_head_limits(_ptr(a), _ptr(b), _ptr(c_), _ptr(g), _ptr(oq), _ptr(ok_), _ptr(ov),
+                                                 nq, nk, d, float(scale),
+                                                 lim.ctypes.data_as(ctypes.POINTER(ctypes.c_long)))
+        _check(rc, "attention_bwd")
         dq[h], dk[h], dv[h] = oq, ok_, ov
-    return dq.reshape(lead + (nq, d)), dk.reshape(lead + (nk, d)), dv.reshape(lead + (nk, d))
+    dq = dq.reshape(lead + (nq, d))
+    dk = dk.reshape(k.shape)
+    dv = dv.reshape(v.shape)
+    if group > 1:  # sum over the query heads that share a key/value head
+        shp = dk.shape[:-3] + (Hkv, group, nk, d)
+        dk, dv = dk.reshape(shp).sum(axis=-3), dv.reshape(shp).sum(axis=-3)
+    return dq, dk, dv
 
 
 def partial_state(q, k, v, scale: float):

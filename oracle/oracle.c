@@ -268,13 +268,18 @@ int fao_decode_splitkv(const double* q, const double* k, const double* v,
  *     dQ = scale dS K,   dK = scale dS^T Q
  *   (the chain rule through S = scale Q K^T; the pages give only dV, the rest is calculus).
  *   q, dq [nq, d]; k, v, dk, dv [nk, d]; dout [nq, d].  Plain loops, O(nq nk d).
+ *   limits[i], if not NULL, is the number of leading keys row i sees (1 .. nk): the other
+ *   keys get P_ij = 0, so they receive no gradient from row i.
  */
-int fao_attention_bwd_head(const double* q, const double* k, const double* v,
-                           const double* dout, double* dq, double* dk, double* dv,
-                           long nq, long nk, long d, double scale)
+int fao_attention_bwd_head_limits(const double* q, const double* k, const double* v,
+                                  const double* dout, double* dq, double* dk, double* dv,
+                                  long nq, long nk, long d, double scale, const long* limits)
 {
     if (nq < 1 || nk < 1 || d < 1) return FAO_BAD_ARG;
     if (!q || !k || !v || !dout || !dq || !dk || !dv) return FAO_BAD_ARG;
+    if (limits)
+        for (long i = 0; i < nq; ++i)
+            if (limits[i] < 1 || limits[i] > nk) return FAO_BAD_ARG;
     double* P = (double*)malloc((size_t)nq * nk * sizeof(double));
     double* orow = (double*)malloc((size_t)d * sizeof(double));
     if (!P || !orow) {
@@ -282,22 +287,24 @@ int fao_attention_bwd_head(const double* q, const double* k, const double* v,
         free(orow);
         return FAO_NO_MEM;
     }
-    for (long i = 0; i < nq; ++i) { /* P row by row: scores, max, exp, normalise */
+    for (long i = 0; i < nq; ++i) { /* P row by row: scores, max, exp, normalise; masked keys get P = 0 */
         double* p = P + i * nk;
-        for (long j = 0; j < nk; ++j) {
+        const long n_i = limits ? limits[i] : nk;
+        for (long j = 0; j < n_i; ++j) {
             double acc = 0.0;
             for (long c = 0; c < d; ++c) acc += q[i * d + c] * k[j * d + c];
             p[j] = scale * acc;
         }
         double m = p[0];
-        for (long j = 1; j < nk; ++j)
+        for (long j = 1; j < n_i; ++j)
             if (p[j] > m) m = p[j];
         double l = 0.0;
-        for (long j = 0; j < nk; ++j) {
+        for (long j = 0; j < n_i; ++j) {
             p[j] = exp(p[j] - m);
             l += p[j];
         }
-        for (long j = 0; j < nk; ++j) p[j] /= l;
+        for (long j = 0; j < n_i; ++j) p[j] /= l;
+        for (long j = n_i; j < nk; ++j) p[j] = 0.0;
     }
     for (long x = 0; x < nq * d; ++x) dq[x] = 0.0;
     for (long x = 0; x < nk * d; ++x) dk[x] = dv[x] = 0.0;
@@ -326,4 +333,12 @@ int fao_attention_bwd_head(const double* q, const double* k, const double* v,
     free(P);
     free(orow);
     return FAO_OK;
+}
+
+/* Unmasked gradients: every query row sees all nk keys. */
+int fao_attention_bwd_head(const double* q, const double* k, const double* v,
+                           const double* dout, double* dq, double* dk, double* dv,
+                           long nq, long nk, long d, double scale)
+{
+    return fao_attention_bwd_head_limits(q, k, v, dout, dq, dk, dv, nq, nk, d, scale, NULL);
 }

@@ -130,3 +130,37 @@ def check_decode(q, k, v, o, lse, scale: float, splits: int, order=None, heads=N
         assert res["lse"] <= tol["lse"], f"{name}: max|dLSE| {res['lse']:.3e}"
     print(f"[parity] {name}: " + " ".join(f"{k}={v:.3e}" for k, v in res.items()))
     return res
+
+
+# Backward tolerances, relative to the size of each gradient tensor (no bound is fixed for the
+# backward elsewhere, so these are derived from its arithmetic).  With bf16 unit roundoff
+# u = 2^-8, every term of dV = P^T dO carries the rounding of P (u) and the output carries one more
+# (u); dQ and dK add the rounding of dS (u) and the error of D = rowsum(dO * O), which is computed
+# from the bf16-rounded forward output (u per term).  A term-wise worst case is therefore about
+# 4u = 1.6e-2 of the largest |gradient| element.  The mean error is about 0.6u for diffuse P; when P
+# is concentrated on one key, dP_ij - D_i cancels and the rounding of O in D dominates dS, which
+# raises the mean error of dQ and dK to about 1.6u (a CPU emulation of the same roundings gives the
+# same figure, and it falls back to 0.6u when O is not rounded).  The mean bound is 2u.
+TOL_BWD = dict(max_rel=4 * 2.0 ** -8, mean_rel=2 * 2.0 ** -8)
+
+
+def check_bwd(q, k, v, dout, dq, dk, dv, scale: float, causal: bool = False, name: str = "") -> dict:
+    """GPU gradients against the oracle's float64 gradients on the same input bytes.
+
+    For each of dQ, dK, dV: max|err| / max|ref| <= TOL_BWD['max_rel'] and
+    mean|err| / mean|ref| <= TOL_BWD['mean_rel'].
+    """
+    ref = oracle.attention_bwd(q, k, v, dout, scale, causal=causal)
+    res = {}
+    for nm, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        g = got.float().cpu().numpy().astype(np.float64)
+        assert g.shape == r.shape, f"{name}: {nm} shape {g.shape} vs {r.shape}"
+        assert np.isfinite(g).all(), f"{name}: non-finite {nm}"
+        err = np.abs(g - r)
+        res[nm + "_max_rel"] = float(err.max() / max(np.abs(r).max(), 1e-30))
+        res[nm + "_mean_rel"] = float(err.mean() / max(np.abs(r).mean(), 1e-30))
+    print(f"[parity] {name}: " + " ".join(f"{k}={v:.3e}" for k, v in res.items()))
+    for nm in ("dq", "dk", "dv"):
+        assert res[nm + "_max_rel"] <= TOL_BWD["max_rel"], f"{name}: {nm} max rel err {res[nm + '_max_rel']:.3e}"
+        assert res[nm + "_mean_rel"] <= TOL_BWD["mean_rel"], f"{name}: {nm} mean rel err {res[nm + '_mean_rel']:.3e}"
+    return res

@@ -172,3 +172,41 @@ def test_fwd_workspace_bytes_explicit_splits():
     # fp32, one split: rounded Q (1*4*100*64*4 = 102400), rounded K (1*2*256*64*4), V^T (1*2*64*256*4)
     assert L.fa_fwd_workspace_bytes(1, 4, 2, 100, 256, 64, fa.FA_FP32, 0, 1) == 102400 + 131072 + 131072
     assert L.fa_fwd_workspace_bytes(1, 4, 3, 100, 256, 64, fa.FA_BF16, 0, 1) == 0  # invalid heads
+
+
+def _bwd(**kw):
+    a = dict(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P2, dk=P2, dv=P2, B=1, H=4, Hkv=2, Nq=100, Nk=256, d=64,
+             scale=0.125, dtype=fa.FA_BF16, causal=0, ws=None, ws_bytes=0)
+    a.update(kw)
+    return fa.lib().fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"],
+                           a["H"], a["Hkv"], a["Nq"], a["Nk"], a["d"], a["scale"], a["dtype"], a["causal"], a["ws"],
+                           a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(do=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(dk=P2 + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=P + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(Hkv=3), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=1, Nq=300), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(ws=P, ws_bytes=16), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=P + 4, ws_bytes=1 << 20), fa.FA_ERR_INVALID_ARG),
+])
+def test_bwd_rejects(kw, status):
+    assert _bwd(**kw) == status
+
+
+def test_bwd_workspace_bytes():
+    L = fa.lib()
+    # D and -LSE log2(e), fp32, Nq rounded up to 64: 1*4*128*4 = 2048 bytes each
+    assert L.fa_bwd_workspace_bytes(1, 4, 100, 64) == 2 * 2048
+    assert L.fa_bwd_workspace_bytes(2, 3, 64, 128) == 2 * 1536
+    assert L.fa_bwd_workspace_bytes(1, 1, 1, 64) == 2 * 256  # 256 bytes rounded to 256
+    assert L.fa_bwd_workspace_bytes(1, 1, 64, 80) == 0
+    assert L.fa_bwd_workspace_bytes(0, 1, 64, 64) == 0

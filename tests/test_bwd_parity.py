@@ -1,0 +1,155 @@
+"""GPU parity of the backward pass (fa_bwd) against the float64 oracle's gradients.
+
+The pages give dV_j += P_ij^T dO_i with P rebuilt from the saved row statistics ("Flash Attention
+代码填空 (Level 2-3)", Exercise 5); dQ and dK follow from the chain rule.  Every case runs the
+library's forward first, so the backward sees the O and LSE it would see in training.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_forward_05_gb300 as fa
+import oracle
+from attention_forward_05_gb300.inputs import make_dout, make_qkv
+from parity import TOL_BWD, check_bwd
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, dout, causal=False, scale=None):
+    d = q.shape[-1]
+    sc = 1 / math.sqrt(d) if scale is None else scale
+    o, lse = fa.fa_fwd(q, k, v, scale=sc, causal=causal)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, dout, lse, scale=sc, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    return sc, o, lse, dq, dk, dv
+
+
+SHAPES = [
+    # B, H, Nq, Nk
+    (1, 2, 128, 128),
+    (1, 1, 200, 300),    # ragged query and key tails
+    (2, 1, 256, 256),
+    (1, 1, 77, 1000),
+    (1, 1, 1, 64),       # one query row
+    (1, 2, 300, 65),     # one key past a tile
+    (1, 1, 513, 129),
+]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bwd_shapes(cuda_device, d, shape):
+    B, H, Nq, Nk = shape
+    q, _, _ = make_qkv(B, H, Nq, 1, d, "bf16", seed=1100 + Nq + d, device=cuda_device)
+    _, k, v = make_qkv(B, H, 1, Nk, d, "bf16", seed=1101 + Nk + d, device=cuda_device)
+    dout = make_dout(B, H, Nq, d, "bf16", seed=1102 + Nq, device=cuda_device)
+    sc, _, _, dq, dk, dv = _run(q, k, v, dout)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, name=f"bwd d{d} {shape}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("shape", [(1, 2, 200, 200), (1, 1, 300, 1000), (1, 2, 513, 513), (1, 1, 1, 77)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bwd_causal(cuda_device, d, shape):
+    B, H, Nq, Nk = shape
+    q, _, _ = make_qkv(B, H, Nq, 1, d, "bf16", seed=1200 + Nq + d, device=cuda_device)
+    _, k, v = make_qkv(B, H, 1, Nk, d, "bf16", seed=1201 + Nk + d, device=cuda_device)
+    dout = make_dout(B, H, Nq, d, "bf16", seed=1202 + Nq, device=cuda_device)
+    sc, _, _, dq, dk, dv = _run(q, k, v, dout, causal=True)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, causal=True, name=f"bwd causal d{d} {shape}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("cfg", [(2, 8, 2, 300, 400, 128), (1, 4, 1, 256, 256, 64)],
+                         ids=lambda c: "B%dH%dHkv%dNq%dNk%dd%d" % c)
+def test_bwd_grouped_query_heads(cuda_device, cfg, causal):
+    """dK, dV of a shared key/value head sum over the query heads that read it."""
+    B, H, Hkv, Nq, Nk, d = cfg
+    q, _, _ = make_qkv(B, H, Nq, 1, d, "bf16", seed=1300 + H, device=cuda_device)
+    _, k, v = make_qkv(B, Hkv, 1, Nk, d, "bf16", seed=1301 + Hkv, device=cuda_device)
+    dout = make_dout(B, H, Nq, d, "bf16", seed=1302, device=cuda_device)
+    sc, _, _, dq, dk, dv = _run(q, k, v, dout, causal=causal)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, causal=causal, name=f"bwd gqa {cfg} causal={causal}")
+
+
+def test_bwd_scales_and_peaked_scores(cuda_device):
+    """Unscaled scores (scale 1) and peaked Q, K: P close to one-hot, dS concentrated."""
+    q, k, v = make_qkv(1, 2, 256, 384, 64, "bf16", seed=1400, qk_mult=3.0, device=cuda_device)
+    dout = make_dout(1, 2, 256, 64, "bf16", seed=1401, device=cuda_device)
+    sc, _, _, dq, dk, dv = _run(q, k, v, dout)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, name="bwd peaked")
+    q, k, v = make_qkv(1, 1, 128, 128, 64, "bf16", seed=1402, qk_mult=0.3, device=cuda_device)
+    dout = make_dout(1, 1, 128, 64, "bf16", seed=1403, device=cuda_device)
+    sc, _, _, dq, dk, dv = _run(q, k, v, dout, scale=1.0)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, name="bwd scale=1")
+
+
+def test_bwd_deterministic_and_caller_workspace(cuda_device):
+    """No atomics: repeated calls are bit-identical, with the library's or the caller's workspace."""
+    q, k, v = make_qkv(2, 4, 700, 900, 64, "bf16", seed=1500, device=cuda_device)
+    dout = make_dout(2, 4, 700, 64, "bf16", seed=1501, device=cuda_device)
+    o, lse = fa.fa_fwd(q, k, v)
+    a = fa.fa_bwd(q, k, v, o, dout, lse)
+    nbytes = fa.fa_bwd_workspace_bytes(2, 4, 700, 64)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=cuda_device)
+    b = fa.fa_bwd(q, k, v, o, dout, lse, workspace=ws)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    with pytest.raises(fa.FAError):
+        fa.fa_bwd(q, k, v, o, dout, lse, workspace=ws[: nbytes - 256])
+
+
+def test_bwd_rejects_fp32(cuda_device):
+    q, k, v = make_qkv(1, 1, 64, 64, 64, "fp32", seed=1600, device=cuda_device)
+    o, lse = fa.fa_fwd(q, k, v)
+    with pytest.raises(fa.FAError) as ei:
+        fa.fa_bwd(q, k, v, o, o.clone(), lse)
+    assert ei.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+def test_bwd_full_size_d64(cuda_device):
+    """B=4 H=16 N=4096 d=64 (the multi-head prefill shape): two whole heads, the first and the
+    last, against the oracle."""
+    B, H, N, d = 4, 16, 4096, 64
+    q, k, v = make_qkv(B, H, N, N, d, "bf16", seed=1003, device=cuda_device)
+    dout = make_dout(B, H, N, d, "bf16", seed=1700, device=cuda_device)
+    sc, _, _, dq, dk, dv = _run(q, k, v, dout)
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        check_bwd(q[sl], k[sl], v[sl], dout[sl], dq[sl], dk[sl], dv[sl], sc, name=f"bwd full d64 head ({b},{h})")
+
+
+def test_bwd_full_size_d128_properties(cuda_device):
+    """B=2 H=16 N=8192 d=128 with peaked scores: dQ on sampled rows against the oracle (a row's dQ
+    needs only that row and all keys), and two identities that hold at any size:
+    sum_j dV_j = sum_i dO_i (rows of P sum to 1) and sum_j dK_j = 0 (sum_j dS_ij = 0 for every i)."""
+    B, H, N, d = 2, 16, 8192, 128
+    q, k, v = make_qkv(B, H, N, N, d, "bf16", seed=1004, qk_mult=3.0, device=cuda_device)
+    dout = make_dout(B, H, N, d, "bf16", seed=1701, device=cuda_device)
+    sc, _, _, dq, dk, dv = _run(q, k, v, dout)
+    rng = np.random.default_rng(1702)
+    rows = np.unique(np.concatenate([[0, 127, 128, N - 1], rng.choice(N, 12, replace=False)]))
+    idx = torch.as_tensor(rows, device=cuda_device)
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        qs = q[b:b + 1, h:h + 1, idx]
+        ref_dq, _, _ = oracle.attention_bwd(qs, k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                                            dout[b:b + 1, h:h + 1, idx], sc)
+        got = dq[b:b + 1, h:h + 1, idx].float().cpu().numpy()
+        err = np.abs(got - ref_dq)
+        rel = err.max() / np.abs(ref_dq).max()
+        print(f"[parity] bwd full d128 dq rows head ({b},{h}): max_rel={rel:.3e}")
+        assert rel <= TOL_BWD["max_rel"]
+    dv64 = dv.double().sum(dim=2)
+    do64 = dout.double().sum(dim=2)
+    e_v = ((dv64 - do64).abs().max() / dout.double().abs().sum(dim=2).max()).item()
+    dk64 = dk.double().sum(dim=2)
+    e_k = (dk64.abs().max() / dk.double().abs().sum(dim=2).max()).item()
+    print(f"[parity] bwd full d128 identities: sum dV vs sum dO {e_v:.3e}, |sum dK| {e_k:.3e}")
+    # each sum has 8192 terms, each carrying a relative rounding of about u = 2^-8
+    assert e_v <= 2.0 ** -8 and e_k <= 2.0 ** -8

@@ -330,29 +330,34 @@ def test_causal_library_and_closed_forms():
     assert np.array_equal(o3, o[:, :, [2, 7]])
 
 
-def test_backward_finite_differences():
-    """dQ, dK, dV against central differences of the loss L = sum(dO * O) in float64 (the oracle's
-    forward): checks every gradient without using its formulas."""
-    rng = np.random.default_rng(16)
-    nq, nk, d, sc = 4, 6, 3, 0.7
-    q, k, v, g = _rand(rng, nq, d), _rand(rng, nk, d), _rand(rng, nk, d), _rand(rng, nq, d)
-    dq, dk, dv = oracle.attention_bwd(q, k, v, g, sc)
+@pytest.mark.parametrize("causal,hkv", [(False, 2), (True, 2), (False, 1), (True, 1)])
+def test_backward_finite_differences(causal, hkv):
+    """dQ, dK, dV against central differences of the loss L = sum(dO * O) through the oracle's own
+    forward (causal mask and shared key/value heads included): checks every gradient without using
+    its formulas."""
+    rng = np.random.default_rng(16 + hkv + 2 * causal)
+    H, nq, nk, d, sc = 2, 4, 6, 3, 0.7
+    q, k, v, g = _rand(rng, 1, H, nq, d), _rand(rng, 1, hkv, nk, d), _rand(rng, 1, hkv, nk, d), _rand(rng, 1, H, nq, d)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, sc, causal=causal)
+    assert dk.shape == k.shape and dv.shape == v.shape
 
     def loss(qq, kk, vv):
-        return float((oracle.attention(qq, kk, vv, sc)[0] * g).sum())
+        return float((oracle.attention(qq, kk, vv, sc, causal=causal)[0] * g).sum())
 
     h = 1e-6
+    args = {"q": q, "k": k, "v": v}
     for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
         num = np.empty_like(x)
         for idx in np.ndindex(x.shape):
             xp, xm = x.copy(), x.copy()
             xp[idx] += h
             xm[idx] -= h
-            args = {"q": q, "k": k, "v": v}
             lp = loss(*(xp if n == name else args[n] for n in ("q", "k", "v")))
             lm = loss(*(xm if n == name else args[n] for n in ("q", "k", "v")))
             num[idx] = (lp - lm) / (2 * h)
         assert np.abs(num - grad).max() <= 1e-8, name
+    if causal:  # the last key is seen by the last query row only
+        assert np.abs(dk[..., nk - 1, :]).max() > 0
 
 
 def test_backward_autograd_library():
