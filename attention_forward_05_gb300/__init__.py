@@ -13,6 +13,7 @@ Entry points (same names as the C ABI):
   fa_decode_splitkv(q, k, v, splits, o=None) -> o
   fa_decode_splitkv_ex(q, k, v, splits, scale=None, workspace=None, merge_order=None, with_lse=False)
   fa_decode_workspace_bytes(B, H, d, splits)
+  fa_decode_splitkv_gqa(q, k, v, splits, scale=None, workspace=None, merge_order=None, with_lse=False)
   fa_bwd(q, k, v, o, dout, lse, scale=None, causal=False, workspace=None) -> (dq, dk, dv)
   fa_bwd_workspace_bytes(B, H, Nq, d)
   fa_check_device_error()
@@ -67,6 +68,8 @@ def lib() -> ctypes.CDLL:
             L.fa_decode_splitkv.restype = i
             L.fa_decode_splitkv_ex.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp, vp, vp]
             L.fa_decode_splitkv_ex.restype = i
+            L.fa_decode_splitkv_gqa.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp, vp]
+            L.fa_decode_splitkv_gqa.restype = i
             L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
             L.fa_decode_workspace_bytes.restype = sz
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
@@ -268,6 +271,47 @@ def fa_decode_splitkv_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, spli
                                     int(splits), float(scale), ws_ptr, ws_bytes, ord_ptr,
                                     lse.data_ptr() if lse is not None else None, _stream_handle(stream))
     _check(st, "fa_decode_splitkv_ex")
+    return o, lse
+
+
+def fa_decode_splitkv_gqa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, splits: int,
+                          scale: float | None = None, workspace: torch.Tensor | None = None,
+                          merge_order: torch.Tensor | None = None, with_lse: bool = False,
+                          o: torch.Tensor | None = None, stream=None):
+    """Split-KV decode with Hkv = k.shape[1] key/value heads shared by q's H query heads; returns (o, lse).
+
+    q [B, H, d] or [B, H, 1, d]; k, v [B, Hkv, Nk, d]; all bf16.
+    """
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda_contig(n, t)
+    if k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("k/v [B,Hkv,Nk,d] expected")
+    B, Hkv, Nk, d = k.shape
+    if q.dim() not in (3, 4) or q.shape[0] != B or q.shape[-1] != d or (q.dim() == 4 and q.shape[2] != 1):
+        raise ValueError("q [B,H,d] or [B,H,1,d] expected")
+    H = q.shape[1]
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise TypeError("decode takes bf16 q, k, v")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, d), device=q.device, dtype=torch.bfloat16)
+    _need_cuda_contig("o", o)
+    lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if with_lse else None
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need_cuda_contig("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    ord_ptr = None
+    if merge_order is not None:
+        _need_cuda_contig("merge_order", merge_order)
+        if merge_order.dtype != torch.int32 or merge_order.numel() != splits:
+            raise ValueError("merge_order must be int32 [splits]")
+        ord_ptr = merge_order.data_ptr()
+    st = lib().fa_decode_splitkv_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, H, Hkv, Nk, d,
+                                     int(splits), float(scale), ws_ptr, ws_bytes, ord_ptr,
+                                     lse.data_ptr() if lse is not None else None, _stream_handle(stream))
+    _check(st, "fa_decode_splitkv_gqa")
     return o, lse
 
 

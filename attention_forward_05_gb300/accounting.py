@@ -46,6 +46,12 @@ def decode_min_bytes(B: int, H: int, Nk: int, d: int, dtype: str = "bf16") -> in
     return 2 * B * H * Nk * d * e + 2 * B * H * d * e
 
 
+def decode_gqa_min_bytes(B: int, H: int, Hkv: int, Nk: int, d: int, dtype: str = "bf16") -> int:
+    """Algorithmic bytes of a grouped-query decode: each key/value head's K and V once, q read, o written."""
+    e = ESIZE[dtype]
+    return 2 * B * Hkv * Nk * d * e + 2 * B * H * d * e
+
+
 def decode_workspace_traffic(B: int, H: int, d: int, splits: int) -> int:
     """Bytes of fp32 partial states (m, l, o[d]) written by the split kernel and read by the merge."""
     return 2 * B * H * splits * (d + 2) * 4

@@ -448,6 +448,60 @@ int fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o, i
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int Nk, int d,
+                          int splits, float scale, void* workspace, size_t workspace_bytes, const int* merge_order,
+                          float* lse, fa_stream_t stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
+  if (merge_order && (reinterpret_cast<uintptr_t>(merge_order) & 3u)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || Nk < 1 || Nk >= (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (splits < 1 || splits > Nk) return FA_ERR_INVALID_ARG;
+  if (splits > 4096) return FA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!fa::decode_gqa_supported_group(H / Hkv)) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH * splits > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * Hkv * static_cast<long long>(Nk) * d > kMaxElems) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_decode_workspace_bytes(B, H, d, splits);
+  if (workspace && (!aligned16(workspace) || workspace_bytes < need)) return FA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  int* err = nullptr;
+  int rc = device_setup(&dev, &err);
+  if (rc != FA_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  if (ws == nullptr) {
+    cudaError_t ea = cudaMallocAsync(&ws, need, st);
+    if (ea != cudaSuccess) return cuda_fail(ea);
+  }
+  fa::DecodeGqaLaunch a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.ws = static_cast<float*>(ws);
+  a.order = merge_order;
+  a.err = err;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Nk = Nk;
+  a.d = d;
+  a.splits = splits;
+  a.c = scale * 1.4426950408889634f;
+  a.stream = st;
+  cudaError_t e = fa::launch_decode_gqa(a);
+  if (workspace == nullptr) {
+    cudaError_t e2 = cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 int fa_decode_splitkv(const void* q, const void* k, const void* v, void* o, int B, int H, int Nk, int d, int splits,
                       fa_stream_t stream) {
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;

@@ -247,6 +247,22 @@ static cudaError_t launch_decode_d(const DecodeLaunch& a) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_decode_merge(const float* ws_m, const float* ws_l, const float* ws_o, const int* order, void* o,
+                                float* lse, int BH, int splits, int d, cudaStream_t stream) {
+  if (splits < 1 || splits > MAX_SPLITS || BH < 1) return cudaErrorInvalidValue;
+  const int heads_per_cta = MERGE_THREADS / 32;
+  const unsigned grid = static_cast<unsigned>((BH + heads_per_cta - 1) / heads_per_cta);
+  if (d == 64)
+    fa_decode_merge_kernel<64><<<grid, MERGE_THREADS, 0, stream>>>(ws_m, ws_l, ws_o, order,
+                                                                  static_cast<__nv_bfloat16*>(o), lse, BH, splits);
+  else if (d == 128)
+    fa_decode_merge_kernel<128><<<grid, MERGE_THREADS, 0, stream>>>(ws_m, ws_l, ws_o, order,
+                                                                   static_cast<__nv_bfloat16*>(o), lse, BH, splits);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeLaunch& a) {
   if (a.splits < 1 || a.splits > MAX_SPLITS) return cudaErrorInvalidValue;
   if (a.d == 64) return launch_decode_d<64>(a);

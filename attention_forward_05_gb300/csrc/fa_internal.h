@@ -108,4 +108,27 @@ struct DecodeLaunch {
 
 cudaError_t launch_decode(const DecodeLaunch& a);
 
+// Merge of per-(head, chunk) decode states in `order` (or 0..splits-1): o = sum w o_s / sum w l_s.
+cudaError_t launch_decode_merge(const float* ws_m, const float* ws_l, const float* ws_o, const int* order, void* o,
+                                float* lse, int BH, int splits, int d, cudaStream_t stream);
+
+struct DecodeGqaLaunch {
+  const void* q;            // [B, H, d] bf16
+  const void* k;            // [B, Hkv, Nk, d] bf16
+  const void* v;
+  void* o;                  // [B, H, d] bf16
+  float* lse;               // [B, H] or nullptr
+  float* ws;                // m [B*H*splits], l [B*H*splits], o [B*H*splits*d]
+  const int* order;         // [splits] or nullptr
+  int* err;                 // device error word
+  int B, H, Hkv, Nk, d, splits;
+  float c;                  // scale * log2(e)
+  cudaStream_t stream;
+};
+
+// 1 when one CTA can serve a group of this many query heads per key/value head (1, 2, 4 or a
+// multiple of 8).
+int decode_gqa_supported_group(int group);
+cudaError_t launch_decode_gqa(const DecodeGqaLaunch& a);
+
 }  // namespace fa

@@ -398,7 +398,7 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if not args.no_extras:
-        line["extras"] = measure_extras(fa, torch, accounting, dev, stream)
+        line["extras"] = measure_extras(fa, torch, accounting, dev, stream, hbm_gbs=peaks["hbm_gbs"])
     if not args.no_cpu_baseline:
         cb_pre, cb_dec = cpu_baseline(args.cpu_seconds)
         line["cpu_baseline"] = cb_pre
@@ -409,14 +409,18 @@ def run_gpu(args):
     return 0
 
 
-def measure_extras(fa, torch, accounting, dev, stream, launches=20):
+def measure_extras(fa, torch, accounting, dev, stream, launches=20, hbm_gbs=None):
     """Rates of the extensions beyond the headline step, each timed alone with CUDA events on
     `stream` after 3 warm-up launches (not part of `value`):
       causal        the two bf16 prefill workloads with the causal mask (visible-key FLOPs)
       gqa           B=4 H=16 N=4096 d=64 bf16 with 2 key/value heads
       split_kv      B=1 H=1 N=4096 d=64 fp32 (TF32) with automatic key splits vs one split
+      decode_gqa    the decode workload (B=32, H=32 query heads, Nk=32768, d=64, 16 splits) with 8 and 4
+                    key/value heads (groups of 4 and 8), GB/s of K/V read once plus q and o
+      bwd           fa_bwd on the two bf16 prefill workloads, plain and causal (FLOPs of the five
+                    backward contractions, 2.5x the forward's)
     """
-    from attention_forward_05_gb300.inputs import WORKLOADS, make_qkv, workload_inputs
+    from attention_forward_05_gb300.inputs import WORKLOADS, make_dout, make_qkv, workload_inputs
 
     def timed(fn):
         for _ in range(3):
@@ -447,6 +451,31 @@ def measure_extras(fa, torch, accounting, dev, stream, launches=20):
     for tag, ks in (("split_kv_auto", 0), ("split_kv_off", 1)):
         ms = timed(lambda: fa.fa_fwd(q, k, v, scale=w.scale, kv_splits=ks, stream=stream))
         out[f"{tag}_long_fp32"] = {"ms": ms, "tflops": fl / ms / 1e9}
+    del q, k, v
+    w = WORKLOADS["decode"]
+    qd, _, _ = make_qkv(w.B, w.H, 1, 1, w.d, "bf16", seed=w.seed, device=dev)
+    for hkv in (8, 4):
+        _, kd, vd = make_qkv(w.B, hkv, 1, w.Nk, w.d, "bf16", seed=w.seed + hkv, device=dev)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.H, w.d, w.splits), dtype=torch.uint8, device=dev)
+        ms = timed(lambda: fa.fa_decode_splitkv_gqa(qd, kd, vd, w.splits, workspace=ws, stream=stream))
+        nbytes = accounting.decode_gqa_min_bytes(w.B, w.H, hkv, w.Nk, w.d)
+        out[f"decode_gqa_hkv{hkv}"] = {"ms": ms, "gbs": nbytes / ms / 1e6, "bytes": nbytes,
+                                       "frac_of_hbm_peak": nbytes / ms / 1e6 / hbm_gbs if hbm_gbs else None}
+        del kd, vd
+    del qd
+    for name in PREFILL:
+        w = WORKLOADS[name]
+        q, k, v = workload_inputs(w, device=dev)
+        dout = make_dout(w.B, w.H, w.Nq, w.d, "bf16", seed=w.seed + 700, device=dev)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
+        for causal in (False, True):
+            o, lse = fa.fa_fwd(q, k, v, scale=w.scale, causal=causal, stream=stream)
+            ms = timed(lambda: fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale, causal=causal, dq=grads[0],
+                                         dk=grads[1], dv=grads[2], workspace=ws, stream=stream))
+            fl = (accounting.bwd_flops_causal if causal else accounting.bwd_flops)(w.B, w.H, w.Nq, w.Nk, w.d)
+            out[f"bwd_{'causal_' if causal else ''}{name}"] = {"ms": ms, "tflops": fl / ms / 1e9}
+        del q, k, v, dout, grads, o, lse
     if fa.fa_check_device_error() != fa.FA_OK:
         raise RuntimeError("device timeout in the extra measurements")
     return out

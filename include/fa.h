@@ -167,8 +167,26 @@ int fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o,
                          void* workspace, size_t workspace_bytes,
                          const int* merge_order, float* lse, fa_stream_t stream);
 
-/* Bytes of fp32 partial-state workspace fa_decode_splitkv_ex needs; 0 on bad arguments. */
+/* Bytes of fp32 partial-state workspace fa_decode_splitkv_ex (and _gqa) needs; 0 on bad arguments. */
 size_t fa_decode_workspace_bytes(int B, int H, int d, int splits);
+
+/*
+ * fa_decode_splitkv_gqa -- split-KV decode where Hkv key/value heads serve H
+ * query heads ("FlashAttention 简化版：Tiling + Online Softmax" §7 names
+ * MQA/GQA): query head h reads key/value head h / (H / Hkv).  Each chunk of
+ * each key/value head is read from device memory once for all the query heads
+ * of its group; the chunk states and their merge are those of
+ * fa_decode_splitkv_ex ([T3] demo 2), one state per (query head, chunk).
+ *   q [B, H, d] bf16, k/v [B, Hkv, Nk, d] bf16, o [B, H, d] bf16 out.
+ *   H / Hkv must be 1, 2, 4 or a multiple of 8 (FA_ERR_UNSUPPORTED otherwise);
+ *   H % Hkv != 0 is FA_ERR_INVALID_ARG.  Other arguments as in
+ *   fa_decode_splitkv_ex; the workspace size is fa_decode_workspace_bytes(B, H,
+ *   d, splits).
+ */
+int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o,
+                          int B, int H, int Hkv, int Nk, int d, int splits, float scale,
+                          void* workspace, size_t workspace_bytes,
+                          const int* merge_order, float* lse, fa_stream_t stream);
 
 /* Size of the fixed device scratch array behind fa_decode_splitkv_noalloc. */
 #define FA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

@@ -210,3 +210,29 @@ def test_bwd_workspace_bytes():
     assert L.fa_bwd_workspace_bytes(1, 1, 1, 64) == 2 * 256  # 256 bytes rounded to 256
     assert L.fa_bwd_workspace_bytes(1, 1, 64, 80) == 0
     assert L.fa_bwd_workspace_bytes(0, 1, 64, 64) == 0
+
+
+def _dec_gqa(**kw):
+    a = dict(q=P, k=P, v=P, o=P2, B=2, H=8, Hkv=2, Nk=64, d=64, splits=4, scale=0.125, ws=None, ws_bytes=0,
+             order=None, lse=None)
+    a.update(kw)
+    return fa.lib().fa_decode_splitkv_gqa(a["q"], a["k"], a["v"], a["o"], a["B"], a["H"], a["Hkv"], a["Nk"], a["d"],
+                                          a["splits"], a["scale"], a["ws"], a["ws_bytes"], a["order"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=None), fa.FA_ERR_INVALID_ARG),
+    (dict(v=P + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(Hkv=3), fa.FA_ERR_INVALID_ARG),     # 8 query heads cannot share 3 key/value heads
+    (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=6, Hkv=2), fa.FA_ERR_UNSUPPORTED),  # groups of 3
+    (dict(H=24, Hkv=2), fa.FA_ERR_UNSUPPORTED),  # groups of 12
+    (dict(splits=0), fa.FA_ERR_INVALID_ARG),
+    (dict(splits=65), fa.FA_ERR_INVALID_ARG),
+    (dict(d=80), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=P, ws_bytes=16), fa.FA_ERR_INVALID_ARG),
+    (dict(order=P + 2), fa.FA_ERR_INVALID_ARG),
+])
+def test_decode_gqa_rejects(kw, status):
+    assert _dec_gqa(**kw) == status
