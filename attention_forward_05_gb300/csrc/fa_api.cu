@@ -368,8 +368,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.nl2 = reinterpret_cast<float*>(ws);
-  a.dvec = reinterpret_cast<float*>(ws + need / 2);
+  a.rowv = reinterpret_cast<float*>(ws);
   a.err = err;
   a.BH = BHi;
   a.BHkv = BHkv;

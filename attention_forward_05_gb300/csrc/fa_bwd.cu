@@ -7,22 +7,25 @@
 
 namespace fa {
 
-// Tile choices.  dK/dV: 128 keys per CTA, 64 query rows per step, ring depth by head size.
+// Tile choices.  dK/dV: 128 keys per CTA, 64 query rows per step; the ring of Q/dO tiles is deep
+// enough that copies land before the MMA warp reaches them (it only refills a stage after the
+// gradient MMAs of the step it held have completed).
 // dQ: two 128-row query tiles per CTA, 64 keys per step.
-using BwdKV64 = BwdKVCfg<64, 64, 4>;
-using BwdKV128 = BwdKVCfg<128, 64, 3>;
+// d=64 uses three score slots in TMEM (512 columns), d=128 two (its dV and dK take 256).
+using BwdKV64 = BwdKVCfg<64, 64, 8, 3>;
+using BwdKV128 = BwdKVCfg<128, 64, 4, 2>;
 using BwdQ64 = BwdQCfg<64, 64, 4>;
 using BwdQ128 = BwdQCfg<128, 64, 2>;
 
-// D_i = sum_c dO_ic O_ic (fp32 over the bf16 inputs) and nl2_i = -L_i log2(e), for the rows of
-// [BH][Nq_pad]; rows i >= Nq get D = 0 and nl2 = -inf, so their P is exactly 0.
+// D_i = sum_c dO_ic O_ic (fp32 over the bf16 inputs) and nl_i = -L_i log2(e) for the rows of
+// [BH][Nq_pad], written interleaved by row pairs: rowv[pair] = (nl_2i, nl_2i+1, D_2i, D_2i+1).
+// Rows i >= Nq get D = 0 and nl = -inf, so their P is exactly 0.
 // A group of D/8 lanes covers one row with 16-byte loads.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __restrict__ o,
                                                           const uint16_t* __restrict__ dout,
-                                                          const float* __restrict__ lse, float* __restrict__ nl2,
-                                                          float* __restrict__ dvec, long long rows_pad, int Nq,
-                                                          int Nq_pad) {
+                                                          const float* __restrict__ lse, float* __restrict__ rowv,
+                                                          long long rows_pad, int Nq, int Nq_pad) {
   constexpr int LPR = D / 8;  // lanes per row
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long r = gt / LPR;
@@ -44,8 +47,9 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
 #pragma unroll
   for (int m = LPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
   if (live && part == 0) {
-    dvec[r] = in_range ? acc : 0.f;
-    nl2[r] = in_range ? -lse[static_cast<size_t>(bh) * Nq + i] * 1.4426950408889634f : -INFINITY;
+    const size_t base = static_cast<size_t>(r - (r & 1)) * 2 + (r & 1);  // Nq_pad is even: pairs stay in a head
+    rowv[base] = in_range ? -lse[static_cast<size_t>(bh) * Nq + i] * 1.4426950408889634f : -INFINITY;
+    rowv[base + 2] = in_range ? acc : 0.f;
   }
 }
 
@@ -56,11 +60,11 @@ cudaError_t launch_bwd_prep(const BwdLaunch& a) {
   if (blocks <= 0 || blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (a.d == 64)
     fa_bwd_prep_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.nl2, a.dvec, rows, a.Nq,
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.rowv, rows, a.Nq,
         a.Nq_pad);
   else
     fa_bwd_prep_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.nl2, a.dvec, rows, a.Nq,
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.rowv, rows, a.Nq,
         a.Nq_pad);
   return cudaGetLastError();
 }
@@ -73,8 +77,7 @@ cudaError_t launch_dkdv(const BwdLaunch& a) {
   BwdKVParams p;
   p.dk = a.dk;
   p.dv = a.dv;
-  p.nl2 = a.nl2;
-  p.dvec = a.dvec;
+  p.rowv = a.rowv;
   p.err = a.err;
   p.Nq = a.Nq;
   p.Nk = a.Nk;
@@ -102,8 +105,7 @@ cudaError_t launch_dq(const BwdLaunch& a) {
   if (e != cudaSuccess) return e;
   BwdQParams p;
   p.dq = a.dq;
-  p.nl2 = a.nl2;
-  p.dvec = a.dvec;
+  p.rowv = a.rowv;
   p.err = a.err;
   p.Nq = a.Nq;
   p.Nk = a.Nk;

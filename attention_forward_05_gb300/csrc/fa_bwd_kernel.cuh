@@ -11,16 +11,18 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three launches, no atomics (the result does not depend on scheduling):
-//   fa_bwd_prep_kernel  D_i and -L_i log2(e) for every query row (padded rows get 0 and -inf).
+//   fa_bwd_prep_kernel  D_i and -L_i log2(e) for every query row (padded rows get 0 and -inf),
+//                       interleaved by row pairs: (nl_2i, nl_2i+1, D_2i, D_2i+1), so one 16-byte
+//                       shared-memory load gives a column pair both values.
 //   fa_bwd_dkdv_kernel  one CTA per (key/value head, 128-key tile); it walks every query tile of every
 //                       query head that shares the key/value head, with S^T and dP^T computed key-major
 //                       (keys on the TMEM lanes), so P^T and dS^T are the tensor-memory A operands of
 //                       dV += P^T dO and dK += dS^T Q.  dV and dK stay in tensor memory throughout.
 //   fa_bwd_dq_kernel    one CTA per two 128-row query tiles; it walks the key tiles, recomputes S and
 //                       dP, and accumulates dQ += dS K with dS read from tensor memory.
-// Both main kernels keep the forward's warp roles: one TMA warp, one MMA-issuing warp, and two
-// warpgroups of thread-per-row elementwise work that alternate so the tensor core is never idle
-// waiting for one of them.
+// Both main kernels keep the forward's warp roles: one TMA warp, one MMA-issuing warp, and
+// warpgroups of thread-per-row elementwise work that take turns, so the tensor core computes the
+// next products while a warpgroup works on the last ones.
 #pragma once
 
 #include "fa_internal.h"
@@ -35,6 +37,16 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint
                : "memory");
 }
 
+// Warp-collective store of 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 template <int NWARPS, int MINB>
 struct RegBudget {  // registers per thread: 16384 per SM sub-partition, shared by ceil(warps/4) warps
   static constexpr int PER_SUB = (NWARPS * MINB + 3) / 4;
@@ -47,12 +59,14 @@ enum : int { WB_KV = 0x21, WB_SF, WB_SE, WB_PF, WB_DONE, WB_Q, WB_KF, WB_VF, WB_
 
 // ------------------------------------------------------------------------------------------ dK, dV
 
-template <int D_, int BQ_, int STAGES_>
+template <int D_, int BQ_, int STAGES_, int NSLOT_>
 struct BwdKVCfg {
   static constexpr int D = D_;
   static constexpr int BK = 128;             // keys per CTA (TMEM lanes, M of every MMA)
   static constexpr int BQ = BQ_;             // query rows per step (N of S^T and dP^T, K of dV and dK)
-  static constexpr int STAGES = STAGES_;     // ring of (Q_i, dO_i, -L_i log2 e, D_i)
+  static constexpr int STAGES = STAGES_;     // ring of (Q_i, dO_i, row values)
+  static constexpr int NSLOT = NSLOT_;       // TMEM slots for (S^T, dP^T); one elementwise warpgroup each
+  static constexpr int LA = NSLOT - 1;       // steps whose scores are issued ahead of the gradient MMAs
   static constexpr int CHUNK = 64;           // bf16 elements per 128-byte swizzled row segment
   static constexpr int NCH = D / CHUNK;
   static constexpr int MMA_K = 16;
@@ -60,29 +74,30 @@ struct BwdKVCfg {
   static constexpr int KV_BYTES = NCH * KV_CH_BYTES;
   static constexpr int QS_CH_BYTES = BQ * 128;
   static constexpr int QS_BYTES = NCH * QS_CH_BYTES;
-  static constexpr int VEC_BYTES = BQ * 4;
+  static constexpr int VEC_BYTES = BQ * 8;   // (-L log2 e, D) of the step's rows, interleaved by pairs
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
   static constexpr int OFF_Q = OFF_V + KV_BYTES;              // stage s at + s * QS_BYTES
   static constexpr int OFF_DO = OFF_Q + STAGES * QS_BYTES;
-  static constexpr int OFF_VEC = OFF_DO + STAGES * QS_BYTES;  // stage s: nl2 at + 2 s VEC, D at + (2 s + 1) VEC
-  static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * VEC_BYTES;
-  // barriers: kv_full, st_full[S], st_empty[S], s_full[2], p_full[2], done, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 4 + 2;
+  static constexpr int OFF_VEC = OFF_DO + STAGES * QS_BYTES;  // stage s at + s * VEC_BYTES
+  static constexpr int OFF_BAR = OFF_VEC + STAGES * VEC_BYTES;
+  // barriers: kv_full, st_full[S], st_empty[S], s_full[NSLOT], p_full[NSLOT], done, drain
+  static constexpr int NBAR = 1 + 2 * STAGES + 2 * NSLOT + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  // TMEM: slot b (b = 0, 1) holds S^T at b*2*BQ and dP^T at b*2*BQ + BQ; P^T and dS^T (bf16 pairs)
-  // are written over the first BQ/2 columns of each.  dV and dK accumulate after the slots.
-  static constexpr int COL_DV = 4 * BQ;
-  static constexpr int COL_DK = 4 * BQ + D;
-  static constexpr int TMEM_NEED = 4 * BQ + 2 * D;
+  // TMEM: slot b holds S^T at b*2*BQ and dP^T at b*2*BQ + BQ; P^T and dS^T (bf16 pairs) are written
+  // over the first BQ/2 columns of each.  dV and dK accumulate after the slots.
+  static constexpr int COL_DV = NSLOT * 2 * BQ;
+  static constexpr int COL_DK = COL_DV + D;
+  static constexpr int TMEM_NEED = NSLOT * 2 * BQ + 2 * D;
   static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
-  static constexpr int NWARPS = 10;
+  static constexpr int NWARPS = 4 * NSLOT + 2;
   static constexpr int NTHREADS = NWARPS * 32;
-  static constexpr int LOAD_WARP = 8;
-  static constexpr int MMA_WARP = 9;
+  static constexpr int LOAD_WARP = 4 * NSLOT;
+  static constexpr int MMA_WARP = 4 * NSLOT + 1;
   static constexpr int MAXREG = RegBudget<NWARPS, 1>::VALUE;
   static_assert(D % CHUNK == 0 && BQ % 32 == 0 && BQ <= 128, "tile");
+  static_assert(NSLOT >= 2 && STAGES >= NSLOT, "the ring must hold the steps issued ahead");
   static_assert(TMEM_NEED <= 512, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(QS_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
@@ -91,8 +106,7 @@ struct BwdKVCfg {
 struct BwdKVParams {
   void* dk;              // [B, Hkv, Nk, D] bf16
   void* dv;
-  const float* nl2;      // [B*H][Nq_pad]: -L_i log2(e), -inf for padded rows
-  const float* dvec;     // [B*H][Nq_pad]: D_i, 0 for padded rows
+  const float* rowv;     // [B*H][Nq_pad/2][4]: (-L log2 e, D) of row pairs; padded rows -inf and 0
   int* err;
   int Nq, Nk, Nq_pad, n_kblk, n_qt;
   int H, Hkv;
@@ -129,9 +143,9 @@ __global__ void __maxnreg__(C::MAXREG)
   auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
   auto bar_sf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + w); };
-  auto bar_pf = [&](int w) { return bar0 + 8u * (3 + 2 * C::STAGES + w); };
-  const uint32_t bar_done = bar0 + 8u * (5 + 2 * C::STAGES);
-  const uint32_t bar_drain = bar0 + 8u * (6 + 2 * C::STAGES);
+  auto bar_pf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + C::NSLOT + w); };
+  const uint32_t bar_done = bar0 + 8u * (1 + 2 * C::STAGES + 2 * C::NSLOT);
+  const uint32_t bar_drain = bar_done + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -141,7 +155,7 @@ __global__ void __maxnreg__(C::MAXREG)
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    for (int w = 0; w < 2; ++w) {
+    for (int w = 0; w < C::NSLOT; ++w) {
       mbar_init(bar_sf(w), 1);
       mbar_init(bar_pf(w), 4);  // one arrive per warp of the warpgroup
     }
@@ -182,7 +196,7 @@ __global__ void __maxnreg__(C::MAXREG)
         if (!mbar_wait(bar_empty(st), ((s / C::STAGES) & 1) ^ 1, abort_flag, p.err, WB_SE)) break;
         const int bh = step_head(s);
         const int q0 = step_qt(s) * C::BQ;
-        mbar_expect_tx(bar_full(st), 2 * C::QS_BYTES + 2 * C::VEC_BYTES);
+        mbar_expect_tx(bar_full(st), 2 * C::QS_BYTES + C::VEC_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
           tma_load_3d(sbase + C::OFF_Q + st * C::QS_BYTES + c * C::QS_CH_BYTES, &tm_q, bar_full(st), c * C::CHUNK,
@@ -190,9 +204,9 @@ __global__ void __maxnreg__(C::MAXREG)
           tma_load_3d(sbase + C::OFF_DO + st * C::QS_BYTES + c * C::QS_CH_BYTES, &tm_do, bar_full(st),
                       c * C::CHUNK, q0, bh);
         }
-        const size_t vo = static_cast<size_t>(bh) * p.Nq_pad + q0;
-        bulk_load_1d(sbase + C::OFF_VEC + st * 2 * C::VEC_BYTES, p.nl2 + vo, C::VEC_BYTES, bar_full(st));
-        bulk_load_1d(sbase + C::OFF_VEC + (st * 2 + 1) * C::VEC_BYTES, p.dvec + vo, C::VEC_BYTES, bar_full(st));
+        // rows q0 .. q0 + BQ - 1 of the interleaved row values: 2 floats per row
+        bulk_load_1d(sbase + C::OFF_VEC + st * C::VEC_BYTES, p.rowv + (static_cast<size_t>(bh) * p.Nq_pad + q0) * 2,
+                     C::VEC_BYTES, bar_full(st));
         n_done = s + 1;
       }
       // drain every copy issued above before the CTA exits
@@ -218,71 +232,82 @@ __global__ void __maxnreg__(C::MAXREG)
     const uint64_t ddom0 = sdesc_sw128(sbase + C::OFF_DO, C::QS_CH_BYTES, 1024); // dO as MN-major B
     auto issue_scores = [&](int s) {
       const int st = s % C::STAGES;
-      const uint32_t col = (s & 1) * 2 * C::BQ;
+      const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
       const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
+      if (elect_one()) {  // one lane issues the whole batch
 #pragma unroll
-      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-        const int e = kk * C::MMA_K;
-        const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        if (elect_one()) mma_ss<0>(tmem + col, dk0 + oa, dqk0 + so + ob, idesc_s, kk > 0);
-      }
+        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+          const int e = kk * C::MMA_K;
+          const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          mma_ss<0>(tmem + col, dk0 + oa, dqk0 + so + ob, idesc_s, kk > 0);
+        }
 #pragma unroll
-      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-        const int e = kk * C::MMA_K;
-        const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        if (elect_one()) mma_ss<0>(tmem + col + C::BQ, dv0 + oa, ddok0 + so + ob, idesc_s, kk > 0);
+        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+          const int e = kk * C::MMA_K;
+          const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          mma_ss<0>(tmem + col + C::BQ, dv0 + oa, ddok0 + so + ob, idesc_s, kk > 0);
+        }
       }
+      __syncwarp();
     };
     auto issue_grads = [&](int s) {
       const int st = s % C::STAGES;
-      const uint32_t col = (s & 1) * 2 * C::BQ;
+      const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
       const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
-        const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
-        if (elect_one())
+        for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+          const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
           mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
                     (s > 0 || kk > 0) ? 1u : 0u);
-      }
+        }
 #pragma unroll
-      for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
-        const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-        if (elect_one())
+        for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+          const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
           mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
                     (s > 0 || kk > 0) ? 1u : 0u);
+        }
       }
+      __syncwarp();
     };
     auto commit = [&](uint32_t bar) {
       if (elect_one()) mma_commit(bar);
       __syncwarp();
     };
+    // Scores run LA = NSLOT - 1 steps ahead of the gradient MMAs: the slot that scores(s + LA) writes
+    // was last read by grads(s - 1), issued one iteration earlier (tcgen05 MMAs of one thread execute
+    // in issue order), after its warpgroup had finished with it.
     bool ok = wait_all(bar_kv, 0, WB_KV);
-    for (int s = 0; ok && s <= T; ++s) {
-      if (s < T) {
-        // slot s & 1 was last read by the gradient MMAs of step s - 2, issued before this point
-        ok = wait_all(bar_full(s % C::STAGES), (s / C::STAGES) & 1, WB_SF);
+    for (int s = 0; ok && s < C::LA && s < T; ++s) {
+      ok = wait_all(bar_full(s % C::STAGES), (s / C::STAGES) & 1, WB_SF);
+      if (!ok) break;
+      tc_fence_after();
+      issue_scores(s);
+      commit(bar_sf(s % C::NSLOT));
+    }
+    for (int s = 0; ok && s < T; ++s) {
+      const int sa = s + C::LA;
+      if (sa < T) {
+        ok = wait_all(bar_full(sa % C::STAGES), (sa / C::STAGES) & 1, WB_SF);
         if (!ok) break;
         tc_fence_after();
-        issue_scores(s);
-        commit(bar_sf(s & 1));
+        issue_scores(sa);
+        commit(bar_sf(sa % C::NSLOT));
       }
-      if (s > 0) {
-        const int r = s - 1;
-        ok = wait_all(bar_pf(r & 1), (r >> 1) & 1, WB_PF);
-        if (!ok) break;
-        tc_fence_after();
-        issue_grads(r);
-        commit(bar_empty(r % C::STAGES));
-      }
+      ok = wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
+      if (!ok) break;
+      tc_fence_after();
+      issue_grads(s);
+      commit(bar_empty(s % C::STAGES));
     }
     if (ok) commit(bar_done);
     commit(bar_drain);
     mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
-    // Warpgroup w handles the steps s with s % 2 == w; thread = key row (TMEM lane).
+    // Warpgroup w handles the steps s with s % NSLOT == w; thread = key row (TMEM lane).
     const int w = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
@@ -292,19 +317,18 @@ __global__ void __maxnreg__(C::MAXREG)
     const uint32_t tdP = tS + C::BQ;
     const uint64_t c2 = f2_pack(p.c, p.c);
     bool ok = true;
-    for (int s = w; s < T; s += 2) {
+    for (int s = w; s < T; s += C::NSLOT) {
       const int st = s % C::STAGES;
-      bool okw = mbar_wait(bar_sf(w), (s >> 1) & 1, abort_flag, p.err, WB_SF);
-      // the stage's vectors came by TMA: observe its completion (already complete) before reading them
+      bool okw = mbar_wait(bar_sf(w), (s / C::NSLOT) & 1, abort_flag, p.err, WB_SF);
+      // the stage's row values came by TMA: observe its completion (already complete) before reading
       okw = okw && mbar_wait(bar_full(st), (s / C::STAGES) & 1, abort_flag, p.err, WB_SF);
       ok = __all_sync(0xffffffffu, okw);
       if (!ok) break;
       tc_fence_after();
-      const float* nl2 = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 2 * C::VEC_BYTES);
-      const float* dv = reinterpret_cast<const float*>(smem + C::OFF_VEC + (st * 2 + 1) * C::VEC_BYTES);
+      const float4* rv = reinterpret_cast<const float4*>(smem + C::OFF_VEC + st * C::VEC_BYTES);
       // causal: query column q (row step_qt(s)*BQ + q) is visible to this key when q >= qmin
-      const int qmin = p.causal ? key - p.causal_off - step_qt(s) * C::BQ : -1;
-      uint32_t pk_p[C::BQ / 64][32], pk_ds[C::BQ / 64][32];
+      const int qmin = p.causal ? key - p.causal_off - step_qt(s) * C::BQ : 0;
+      const bool masked = __any_sync(0xffffffffu, qmin > 0);
 #pragma unroll
       for (int cc = 0; cc < C::BQ / 32; ++cc) {
         uint32_t sr[32], dr[32];
@@ -313,32 +337,31 @@ __global__ void __maxnreg__(C::MAXREG)
         tmem_wait_ld();
         reg_fence(sr);
         reg_fence(dr);
+        uint32_t pk_p[16], pk_ds[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const int q = cc * 32 + e;
-          const float2 nl = *reinterpret_cast<const float2*>(nl2 + q);
-          const float2 dd = *reinterpret_cast<const float2*>(dv + q);
+          const float4 vv = rv[q / 2];  // (-L log2 e, D) of columns q and q + 1
           const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
-                                    f2_pack(nl.x, nl.y));
+                                    f2_pack(vv.x, vv.y));
           float x0, x1;
           f2_unpack_f(x, x0, x1);
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (q < qmin) p0 = 0.f;
-          if (q + 1 < qmin) p1 = 0.f;
+          if (masked) {
+            if (q < qmin) p0 = 0.f;
+            if (q + 1 < qmin) p1 = 0.f;
+          }
           const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                    f2_pack(-dd.x, -dd.y));
+                                    f2_pack(-vv.z, -vv.w));
           const uint64_t ds = f2_mul(f2_pack(p0, p1), t);
           float ds0, ds1;
           f2_unpack_f(ds, ds0, ds1);
-          const int word = q / 2;
-          pk_p[word / 32][word % 32] = pack_bf16x2(p0, p1);
-          pk_ds[word / 32][word % 32] = pack_bf16x2(ds0, ds1);
+          pk_p[e / 2] = pack_bf16x2(p0, p1);
+          pk_ds[e / 2] = pack_bf16x2(ds0, ds1);
         }
-      }
-#pragma unroll
-      for (int i = 0; i < C::BQ / 64; ++i) {
-        tmem_st32(tS + i * 32, pk_p[i]);
-        tmem_st32(tdP + i * 32, pk_ds[i]);
+        // chunk cc's packed values go to columns 16 cc .. 16 cc + 15, all read already
+        tmem_st16(tS + cc * 16, pk_p);
+        tmem_st16(tdP + cc * 16, pk_ds);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -346,7 +369,7 @@ __global__ void __maxnreg__(C::MAXREG)
       if (lane == 0) mbar_arrive(bar_pf(w));
     }
     // ---------------------------------------------------------- epilogue: warpgroup 0 writes dV, 1 writes dK
-    bool okd = ok && mbar_wait(bar_done, 0, abort_flag, p.err, WB_DONE);
+    bool okd = ok && w < 2 && mbar_wait(bar_done, 0, abort_flag, p.err, WB_DONE);
     okd = __all_sync(0xffffffffu, okd);
     if (okd) {
       tc_fence_after();
@@ -428,8 +451,7 @@ struct BwdQCfg {
 
 struct BwdQParams {
   void* dq;              // [B, H, Nq, D] bf16
-  const float* nl2;      // [B*H][Nq_pad]
-  const float* dvec;     // [B*H][Nq_pad]
+  const float* rowv;     // [B*H][Nq_pad/2][4]: (-L log2 e, D) of row pairs
   int* err;
   int Nq, Nk, Nq_pad, n_qblk;
   int H, Hkv;
@@ -559,31 +581,36 @@ __global__ void __maxnreg__(C::MAXREG)
       const uint32_t col = t * 2 * C::BC;
       const uint64_t to = static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
       const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+      if (elect_one()) {  // one lane issues the whole batch
 #pragma unroll
-      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-        const int e = kk * C::MMA_K;
-        const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        if (elect_one()) mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
-      }
+        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+          const int e = kk * C::MMA_K;
+          const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
+        }
 #pragma unroll
-      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-        const int e = kk * C::MMA_K;
-        const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-        if (elect_one()) mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
+        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+          const int e = kk * C::MMA_K;
+          const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+          mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
+        }
       }
+      __syncwarp();
     };
     auto issue_dq = [&](int t, int s, bool acc) {
       const uint32_t a_tmem = tmem + t * 2 * C::BC;
       const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
-        const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-        if (elect_one())
+        for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
+          const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
           mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
                     (acc || kk > 0) ? 1u : 0u);
+        }
       }
+      __syncwarp();
     };
     auto commit = [&](uint32_t bar) {
       if (elect_one()) mma_commit(bar);
@@ -635,9 +662,9 @@ __global__ void __maxnreg__(C::MAXREG)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 2 * C::BC;
     const uint32_t tdP = tS + C::BC;
-    const size_t vrow = static_cast<size_t>(bh) * p.Nq_pad + qrow;
-    const float nl = in_range ? p.nl2[vrow] : -INFINITY;
-    const float dd = in_range ? p.dvec[vrow] : 0.f;
+    const size_t vpair = (static_cast<size_t>(bh) * p.Nq_pad + (qrow & ~1)) * 2;  // float index of the row pair
+    const float nl = in_range ? p.rowv[vpair + (qrow & 1)] : -INFINITY;
+    const float dd = in_range ? p.rowv[vpair + 2 + (qrow & 1)] : 0.f;
     const int row_lim = p.causal ? min(p.Nk, qrow + 1 + p.causal_off) : p.Nk;  // keys [0, row_lim) visible
     const uint64_t c2 = f2_pack(p.c, p.c);
     const uint64_t nl_2 = f2_pack(nl, nl);
