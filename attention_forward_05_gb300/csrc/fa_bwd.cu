@@ -18,7 +18,8 @@ using BwdQ64 = BwdQCfg<64, 64, 4>;
 using BwdQ128 = BwdQCfg<128, 64, 2>;
 
 // D_i = sum_c dO_ic O_ic (fp32 over the bf16 inputs) and nl_i = -L_i log2(e) for the rows of
-// [BH][Nq_pad], written interleaved by row pairs: rowv[pair] = (nl_2i, nl_2i+1, D_2i, D_2i+1).
+// [BH][Nq_pad], written interleaved by row pairs: rowv[pair] = (nl_2i, nl_2i+1, -D_2i, -D_2i+1)
+// (negated, so the kernels form dP - D with one add).
 // Rows i >= Nq get D = 0 and nl = -inf, so their P is exactly 0.
 // A group of D/8 lanes covers one row with 16-byte loads.
 template <int D>
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
   if (live && part == 0) {
     const size_t base = static_cast<size_t>(r - (r & 1)) * 2 + (r & 1);  // Nq_pad is even: pairs stay in a head
     rowv[base] = in_range ? -lse[static_cast<size_t>(bh) * Nq + i] * 1.4426950408889634f : -INFINITY;
-    rowv[base + 2] = in_range ? acc : 0.f;
+    rowv[base + 2] = in_range ? -acc : 0.f;
   }
 }
 

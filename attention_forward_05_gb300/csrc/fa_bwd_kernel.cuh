@@ -11,8 +11,8 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three launches, no atomics (the result does not depend on scheduling):
-//   fa_bwd_prep_kernel  D_i and -L_i log2(e) for every query row (padded rows get 0 and -inf),
-//                       interleaved by row pairs: (nl_2i, nl_2i+1, D_2i, D_2i+1), so one 16-byte
+//   fa_bwd_prep_kernel  -L_i log2(e) and -D_i for every query row (padded rows get -inf and 0),
+//                       interleaved by row pairs: (nl_2i, nl_2i+1, -D_2i, -D_2i+1), so one 16-byte
 //                       shared-memory load gives a column pair both values.
 //   fa_bwd_dkdv_kernel  one CTA per (key/value head, 128-key tile); it walks every query tile of every
 //                       query head that shares the key/value head, with S^T and dP^T computed key-major
@@ -47,6 +47,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// Non-blocking test of an mbarrier phase (no suspend); true when the phase with this parity completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 template <int NWARPS, int MINB>
 struct RegBudget {  // registers per thread: 16384 per SM sub-partition, shared by ceil(warps/4) warps
   static constexpr int PER_SUB = (NWARPS * MINB + 3) / 4;
@@ -66,7 +79,6 @@ struct BwdKVCfg {
   static constexpr int BQ = BQ_;             // query rows per step (N of S^T and dP^T, K of dV and dK)
   static constexpr int STAGES = STAGES_;     // ring of (Q_i, dO_i, row values)
   static constexpr int NSLOT = NSLOT_;       // TMEM slots for (S^T, dP^T); one elementwise warpgroup each
-  static constexpr int LA = NSLOT - 1;       // steps whose scores are issued ahead of the gradient MMAs
   static constexpr int CHUNK = 64;           // bf16 elements per 128-byte swizzled row segment
   static constexpr int NCH = D / CHUNK;
   static constexpr int MMA_K = 16;
@@ -74,15 +86,16 @@ struct BwdKVCfg {
   static constexpr int KV_BYTES = NCH * KV_CH_BYTES;
   static constexpr int QS_CH_BYTES = BQ * 128;
   static constexpr int QS_BYTES = NCH * QS_CH_BYTES;
-  static constexpr int VEC_BYTES = BQ * 8;   // (-L log2 e, D) of the step's rows, interleaved by pairs
+  static constexpr int VEC_BYTES = BQ * 8;   // (-L log2 e, -D) of the step's rows, interleaved by pairs
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
   static constexpr int OFF_Q = OFF_V + KV_BYTES;              // stage s at + s * QS_BYTES
   static constexpr int OFF_DO = OFF_Q + STAGES * QS_BYTES;
   static constexpr int OFF_VEC = OFF_DO + STAGES * QS_BYTES;  // stage s at + s * VEC_BYTES
   static constexpr int OFF_BAR = OFF_VEC + STAGES * VEC_BYTES;
-  // barriers: kv_full, st_full[S], st_empty[S], s_full[NSLOT], p_full[NSLOT], done, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 * NSLOT + 2;
+  // barriers: kv_full, st_full[S], st_empty[S], s_full[NSLOT], p_full[NSLOT], g_free[NSLOT], done,
+  // drain (score issuer), drain (gradient issuer)
+  static constexpr int NBAR = 1 + 2 * STAGES + 3 * NSLOT + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM: slot b holds S^T at b*2*BQ and dP^T at b*2*BQ + BQ; P^T and dS^T (bf16 pairs) are written
@@ -91,13 +104,17 @@ struct BwdKVCfg {
   static constexpr int COL_DK = COL_DV + D;
   static constexpr int TMEM_NEED = NSLOT * 2 * BQ + 2 * D;
   static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
-  static constexpr int NWARPS = 4 * NSLOT + 2;
+  // Two MMA-issuing warps on different SM sub-partitions: one thread issues each tcgen05.mma in
+  // about 44 cycles, longer than an M=128, N=64 product takes, so one issuer cannot keep the tensor
+  // core busy with these shapes and two can.
+  static constexpr int NWARPS = 4 * NSLOT + 3;
   static constexpr int NTHREADS = NWARPS * 32;
   static constexpr int LOAD_WARP = 4 * NSLOT;
-  static constexpr int MMA_WARP = 4 * NSLOT + 1;
+  static constexpr int MMA_WARP = 4 * NSLOT + 1;   // S^T, dP^T
+  static constexpr int GRAD_WARP = 4 * NSLOT + 2;  // dV, dK
   static constexpr int MAXREG = RegBudget<NWARPS, 1>::VALUE;
   static_assert(D % CHUNK == 0 && BQ % 32 == 0 && BQ <= 128, "tile");
-  static_assert(NSLOT >= 2 && STAGES >= NSLOT, "the ring must hold the steps issued ahead");
+  static_assert(NSLOT >= 2 && STAGES >= NSLOT, "the ring must hold the steps in flight");
   static_assert(TMEM_NEED <= 512, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(QS_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
@@ -106,7 +123,7 @@ struct BwdKVCfg {
 struct BwdKVParams {
   void* dk;              // [B, Hkv, Nk, D] bf16
   void* dv;
-  const float* rowv;     // [B*H][Nq_pad/2][4]: (-L log2 e, D) of row pairs; padded rows -inf and 0
+  const float* rowv;     // [B*H][Nq_pad/2][4]: (-L log2 e, -D) of row pairs; padded rows -inf and 0
   int* err;
   int Nq, Nk, Nq_pad, n_kblk, n_qt;
   int H, Hkv;
@@ -114,6 +131,46 @@ struct BwdKVParams {
   float c;                 // scale * log2(e)
   float scale;
 };
+
+// One step of a dK/dV elementwise thread (one key row, BQ query columns): P^T = 2^(s c - L log2 e),
+// dS^T = P^T (dP^T - D), both written back over S^T and dP^T as bf16 pairs.  rv holds the step's
+// (-L log2 e, -D) by column pairs.  MASK: columns q < qmin are above the causal diagonal (P = 0).
+template <class C, bool MASK>
+__device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, const float4* rv, uint64_t c2, int qmin) {
+#pragma unroll
+  for (int cc = 0; cc < C::BQ / 32; ++cc) {
+    uint32_t sr[32], dr[32];
+    tmem_ld32(tS + cc * 32, sr);
+    tmem_ld32(tdP + cc * 32, dr);
+    tmem_wait_ld();
+    reg_fence(sr);
+    reg_fence(dr);
+    uint32_t pk_p[16], pk_ds[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int q = cc * 32 + e;
+      const float4 vv = rv[q / 2];  // (-L log2 e, -D) of columns q and q + 1
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+                                f2_pack(vv.x, vv.y));
+      float x0, x1;
+      f2_unpack_f(x, x0, x1);
+      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if (MASK) {
+        if (q < qmin) p0 = 0.f;
+        if (q + 1 < qmin) p1 = 0.f;
+      }
+      const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(vv.z, vv.w));
+      const uint64_t ds = f2_mul(f2_pack(p0, p1), t);
+      float ds0, ds1;
+      f2_unpack_f(ds, ds0, ds1);
+      pk_p[e / 2] = pack_bf16x2(p0, p1);
+      pk_ds[e / 2] = pack_bf16x2(ds0, ds1);
+    }
+    // chunk cc's packed values go to columns 16 cc .. 16 cc + 15, all read already
+    tmem_st16(tS + cc * 16, pk_p);
+    tmem_st16(tdP + cc * 16, pk_ds);
+  }
+}
 
 template <class C>
 __global__ void __maxnreg__(C::MAXREG)
@@ -144,8 +201,10 @@ __global__ void __maxnreg__(C::MAXREG)
   auto bar_empty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
   auto bar_sf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + w); };
   auto bar_pf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + C::NSLOT + w); };
-  const uint32_t bar_done = bar0 + 8u * (1 + 2 * C::STAGES + 2 * C::NSLOT);
+  auto bar_gf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + 2 * C::NSLOT + w); };
+  const uint32_t bar_done = bar0 + 8u * (1 + 2 * C::STAGES + 3 * C::NSLOT);
   const uint32_t bar_drain = bar_done + 8u;
+  const uint32_t bar_drain_g = bar_done + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -158,9 +217,11 @@ __global__ void __maxnreg__(C::MAXREG)
     for (int w = 0; w < C::NSLOT; ++w) {
       mbar_init(bar_sf(w), 1);
       mbar_init(bar_pf(w), 4);  // one arrive per warp of the warpgroup
+      mbar_init(bar_gf(w), 1);
     }
     mbar_init(bar_done, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_drain_g, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -217,94 +278,90 @@ __global__ void __maxnreg__(C::MAXREG)
         if (cnt > 0) mbar_wait_drain(bar_full(st), (cnt - 1) & 1, p.err, WB_DRAIN);
       }
     }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer (whole warp, elected issue)
+  } else if (warp == C::MMA_WARP || warp == C::GRAD_WARP) {
+    // ------------------------------------------------------------ MMA issuers (whole warp, elected issue)
+    // A phase that already completed is seen by one non-blocking test; only otherwise does the warp
+    // enter the bounded wait.
     auto wait_all = [&](uint32_t bar, uint32_t parity, int where) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where));
-    };
-    constexpr uint32_t idesc_s = make_idesc(1, C::BK, C::BQ, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
-    constexpr uint32_t idesc_g = make_idesc(1, C::BK, C::D, 0, 1);   // dV += P^T dO, dK += dS^T Q (B MN-major)
-    const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-    const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
-    const uint64_t dqk0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);               // Q as K-major B
-    const uint64_t ddok0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);             // dO as K-major B
-    const uint64_t dqm0 = sdesc_sw128(sbase + C::OFF_Q, C::QS_CH_BYTES, 1024);   // Q as MN-major B
-    const uint64_t ddom0 = sdesc_sw128(sbase + C::OFF_DO, C::QS_CH_BYTES, 1024); // dO as MN-major B
-    auto issue_scores = [&](int s) {
-      const int st = s % C::STAGES;
-      const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
-      const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
-      if (elect_one()) {  // one lane issues the whole batch
-#pragma unroll
-        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-          const int e = kk * C::MMA_K;
-          const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          mma_ss<0>(tmem + col, dk0 + oa, dqk0 + so + ob, idesc_s, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-          const int e = kk * C::MMA_K;
-          const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          mma_ss<0>(tmem + col + C::BQ, dv0 + oa, ddok0 + so + ob, idesc_s, kk > 0);
-        }
-      }
-      __syncwarp();
-    };
-    auto issue_grads = [&](int s) {
-      const int st = s % C::STAGES;
-      const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
-      const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
-          const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
-          mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
-                    (s > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
-          const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-          mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
-                    (s > 0 || kk > 0) ? 1u : 0u);
-        }
-      }
-      __syncwarp();
+      if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where)) != 0;
     };
     auto commit = [&](uint32_t bar) {
       if (elect_one()) mma_commit(bar);
       __syncwarp();
     };
-    // Scores run LA = NSLOT - 1 steps ahead of the gradient MMAs: the slot that scores(s + LA) writes
-    // was last read by grads(s - 1), issued one iteration earlier (tcgen05 MMAs of one thread execute
-    // in issue order), after its warpgroup had finished with it.
     bool ok = wait_all(bar_kv, 0, WB_KV);
-    for (int s = 0; ok && s < C::LA && s < T; ++s) {
-      ok = wait_all(bar_full(s % C::STAGES), (s / C::STAGES) & 1, WB_SF);
-      if (!ok) break;
-      tc_fence_after();
-      issue_scores(s);
-      commit(bar_sf(s % C::NSLOT));
-    }
-    for (int s = 0; ok && s < T; ++s) {
-      const int sa = s + C::LA;
-      if (sa < T) {
-        ok = wait_all(bar_full(sa % C::STAGES), (sa / C::STAGES) & 1, WB_SF);
+    if (warp == C::MMA_WARP) {
+      // S^T = K Q^T and dP^T = V dO^T of step s into slot s % NSLOT, as soon as the step's tiles have
+      // landed and the gradient MMAs of step s - NSLOT (the slot's previous user) have completed.
+      constexpr uint32_t idesc_s = make_idesc(1, C::BK, C::BQ, 0, 0);
+      const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      const uint64_t dqk0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);    // Q as K-major B
+      const uint64_t ddok0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);  // dO as K-major B
+      for (int s = 0; ok && s < T; ++s) {
+        ok = wait_all(bar_full(s % C::STAGES), (s / C::STAGES) & 1, WB_SF);
+        if (ok && s >= C::NSLOT) ok = wait_all(bar_gf(s % C::NSLOT), ((s / C::NSLOT) - 1) & 1, WB_PF);
         if (!ok) break;
         tc_fence_after();
-        issue_scores(sa);
-        commit(bar_sf(sa % C::NSLOT));
+        const int st = s % C::STAGES;
+        const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
+        const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
+        if (elect_one()) {  // one lane issues the whole batch
+#pragma unroll
+          for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+            const int e = kk * C::MMA_K;
+            const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+            const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+            mma_ss<0>(tmem + col, dk0 + oa, dqk0 + so + ob, idesc_s, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+            const int e = kk * C::MMA_K;
+            const uint32_t oa = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+            const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+            mma_ss<0>(tmem + col + C::BQ, dv0 + oa, ddok0 + so + ob, idesc_s, kk > 0);
+          }
+        }
+        __syncwarp();
+        commit(bar_sf(s % C::NSLOT));
       }
-      ok = wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
-      if (!ok) break;
-      tc_fence_after();
-      issue_grads(s);
-      commit(bar_empty(s % C::STAGES));
+      commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
+    } else {
+      // dV += P^T dO and dK += dS^T Q of step s once its warpgroup has written P^T and dS^T.
+      constexpr uint32_t idesc_g = make_idesc(1, C::BK, C::D, 0, 1);   // B MN-major
+      const uint64_t dqm0 = sdesc_sw128(sbase + C::OFF_Q, C::QS_CH_BYTES, 1024);   // Q as MN-major B
+      const uint64_t ddom0 = sdesc_sw128(sbase + C::OFF_DO, C::QS_CH_BYTES, 1024); // dO as MN-major B
+      for (int s = 0; ok && s < T; ++s) {
+        ok = wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
+        if (!ok) break;
+        tc_fence_after();
+        const int st = s % C::STAGES;
+        const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
+        const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+            const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
+            mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+            const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+            mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+        commit(bar_gf(s % C::NSLOT));       // the slot may be overwritten
+        commit(bar_empty(s % C::STAGES));   // the stage may be refilled (its score MMAs completed earlier)
+      }
+      if (ok) commit(bar_done);
+      commit(bar_drain_g);
+      mbar_wait_drain(bar_drain_g, 0, p.err, WB_DRAIN);
     }
-    if (ok) commit(bar_done);
-    commit(bar_drain);
-    mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
     // Warpgroup w handles the steps s with s % NSLOT == w; thread = key row (TMEM lane).
@@ -328,41 +385,10 @@ __global__ void __maxnreg__(C::MAXREG)
       const float4* rv = reinterpret_cast<const float4*>(smem + C::OFF_VEC + st * C::VEC_BYTES);
       // causal: query column q (row step_qt(s)*BQ + q) is visible to this key when q >= qmin
       const int qmin = p.causal ? key - p.causal_off - step_qt(s) * C::BQ : 0;
-      const bool masked = __any_sync(0xffffffffu, qmin > 0);
-#pragma unroll
-      for (int cc = 0; cc < C::BQ / 32; ++cc) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + cc * 32, sr);
-        tmem_ld32(tdP + cc * 32, dr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(dr);
-        uint32_t pk_p[16], pk_ds[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int q = cc * 32 + e;
-          const float4 vv = rv[q / 2];  // (-L log2 e, D) of columns q and q + 1
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
-                                    f2_pack(vv.x, vv.y));
-          float x0, x1;
-          f2_unpack_f(x, x0, x1);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (masked) {
-            if (q < qmin) p0 = 0.f;
-            if (q + 1 < qmin) p1 = 0.f;
-          }
-          const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                    f2_pack(-vv.z, -vv.w));
-          const uint64_t ds = f2_mul(f2_pack(p0, p1), t);
-          float ds0, ds1;
-          f2_unpack_f(ds, ds0, ds1);
-          pk_p[e / 2] = pack_bf16x2(p0, p1);
-          pk_ds[e / 2] = pack_bf16x2(ds0, ds1);
-        }
-        // chunk cc's packed values go to columns 16 cc .. 16 cc + 15, all read already
-        tmem_st16(tS + cc * 16, pk_p);
-        tmem_st16(tdP + cc * 16, pk_ds);
-      }
+      if (__any_sync(0xffffffffu, qmin > 0))
+        dkdv_elementwise<C, true>(tS, tdP, rv, c2, qmin);
+      else
+        dkdv_elementwise<C, false>(tS, tdP, rv, c2, qmin);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -451,13 +477,50 @@ struct BwdQCfg {
 
 struct BwdQParams {
   void* dq;              // [B, H, Nq, D] bf16
-  const float* rowv;     // [B*H][Nq_pad/2][4]: (-L log2 e, D) of row pairs
+  const float* rowv;     // [B*H][Nq_pad/2][4]: (-L log2 e, -D) of row pairs
   int* err;
   int Nq, Nk, Nq_pad, n_qblk;
   int H, Hkv;
   int causal, causal_off;
   float c, scale;
 };
+
+// One step of a dQ elementwise thread (one query row, BC key columns): P = 2^(s c - L log2 e),
+// dS = P (dP - D), written back over S as bf16 pairs.  TAIL: columns >= valid are masked (P = 0).
+template <class C, bool TAIL>
+__device__ __forceinline__ void dq_elementwise(uint32_t tS, uint32_t tdP, uint64_t c2, uint64_t nl_2, uint64_t nd_2,
+                                               int valid) {
+  uint32_t pk[C::BC / 64][32];
+#pragma unroll
+  for (int cc = 0; cc < C::BC / 32; ++cc) {
+    uint32_t sr[32], dr[32];
+    tmem_ld32(tS + cc * 32, sr);
+    tmem_ld32(tdP + cc * 32, dr);
+    tmem_wait_ld();
+    reg_fence(sr);
+    reg_fence(dr);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int col = cc * 32 + e;
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nl_2);
+      float x0, x1;
+      f2_unpack_f(x, x0, x1);
+      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if (TAIL) {
+        if (col >= valid) p0 = 0.f;
+        if (col + 1 >= valid) p1 = 0.f;
+      }
+      const uint64_t tt = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd_2);
+      const uint64_t ds = f2_mul(f2_pack(p0, p1), tt);
+      float ds0, ds1;
+      f2_unpack_f(ds, ds0, ds1);
+      const int word = col / 2;
+      pk[word / 32][word % 32] = pack_bf16x2(ds0, ds1);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < C::BC / 64; ++i) tmem_st32(tS + i * 32, pk[i]);
+}
 
 template <class C>
 __global__ void __maxnreg__(C::MAXREG)
@@ -567,8 +630,11 @@ __global__ void __maxnreg__(C::MAXREG)
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
+    // A phase that already completed is seen by one non-blocking test; only otherwise does the warp
+    // enter the bounded wait.  The MMA queue is short, so time spent here idles the tensor core.
     auto wait_all = [&](uint32_t bar, uint32_t parity, int where) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where));
+      if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where)) != 0;
     };
     constexpr uint32_t idesc_s = make_idesc(1, C::BR, C::BC, 0, 0);  // S = Q K^T, dP = dO V^T
     constexpr uint32_t idesc_g = make_idesc(1, C::BR, C::D, 0, 1);   // dQ += dS K (K MN-major)
@@ -664,46 +730,22 @@ __global__ void __maxnreg__(C::MAXREG)
     const uint32_t tdP = tS + C::BC;
     const size_t vpair = (static_cast<size_t>(bh) * p.Nq_pad + (qrow & ~1)) * 2;  // float index of the row pair
     const float nl = in_range ? p.rowv[vpair + (qrow & 1)] : -INFINITY;
-    const float dd = in_range ? p.rowv[vpair + 2 + (qrow & 1)] : 0.f;
+    const float ndd = in_range ? p.rowv[vpair + 2 + (qrow & 1)] : 0.f;  // -D
     const int row_lim = p.causal ? min(p.Nk, qrow + 1 + p.causal_off) : p.Nk;  // keys [0, row_lim) visible
     const uint64_t c2 = f2_pack(p.c, p.c);
     const uint64_t nl_2 = f2_pack(nl, nl);
-    const uint64_t nd_2 = f2_pack(-dd, -dd);
+    const uint64_t nd_2 = f2_pack(ndd, ndd);
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, WB_SF);
       ok = __all_sync(0xffffffffu, okw);
       if (!ok) break;
       tc_fence_after();
-      const int valid = row_lim - j * C::BC;
-      uint32_t pk[C::BC / 64][32];
-#pragma unroll
-      for (int cc = 0; cc < C::BC / 32; ++cc) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tS + cc * 32, sr);
-        tmem_ld32(tdP + cc * 32, dr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(dr);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = cc * 32 + e;
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nl_2);
-          float x0, x1;
-          f2_unpack_f(x, x0, x1);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (col >= valid) p0 = 0.f;
-          if (col + 1 >= valid) p1 = 0.f;
-          const uint64_t tt = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd_2);
-          const uint64_t ds = f2_mul(f2_pack(p0, p1), tt);
-          float ds0, ds1;
-          f2_unpack_f(ds, ds0, ds1);
-          const int word = col / 2;
-          pk[word / 32][word % 32] = pack_bf16x2(ds0, ds1);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < C::BC / 64; ++i) tmem_st32(tS + i * 32, pk[i]);
+      const int valid = row_lim - j * C::BC;  // key columns of this step the row may see
+      if (__all_sync(0xffffffffu, valid >= C::BC))
+        dq_elementwise<C, false>(tS, tdP, c2, nl_2, nd_2, valid);
+      else
+        dq_elementwise<C, true>(tS, tdP, c2, nl_2, nd_2, valid);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

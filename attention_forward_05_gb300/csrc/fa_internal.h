@@ -71,7 +71,7 @@ struct BwdLaunch {
   void* dq;                 // [BH, Nq, d] bf16
   void* dk;                 // [BHkv, Nk, d] bf16
   void* dv;
-  float* rowv;              // workspace [BH][Nq_pad/2][4]: (-L log2 e, D) interleaved by row pairs
+  float* rowv;              // workspace [BH][Nq_pad/2][4]: (-L log2 e, -D) interleaved by row pairs
   int* err;
   int BH, BHkv, H, Hkv, Nq, Nk, Nq_pad, d;
   int causal;
