@@ -334,7 +334,8 @@ __global__ void __maxnreg__(C::MAXREG)
       const uint64_t dqm0 = sdesc_sw128(sbase + C::OFF_Q, C::QS_CH_BYTES, 1024);   // Q as MN-major B
       const uint64_t ddom0 = sdesc_sw128(sbase + C::OFF_DO, C::QS_CH_BYTES, 1024); // dO as MN-major B
       for (int s = 0; ok && s < T; ++s) {
-        ok = wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
+        ok = wait_all(bar_full(s % C::STAGES), (s / C::STAGES) & 1, WB_SF);  // complete already
+        ok = ok && wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
         if (!ok) break;
         tc_fence_after();
         const int st = s % C::STAGES;
@@ -456,8 +457,9 @@ struct BwdQCfg {
   static constexpr int OFF_K = OFF_DO + NQT * Q_BYTES;         // stage s at + s * KV_BYTES
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT], drain
-  static constexpr int NBAR = 1 + 4 * STAGES + 3 * NQT + 1;
+  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT],
+  // g_free[NQT], drain (score issuer), drain (dQ issuer)
+  static constexpr int NBAR = 1 + 4 * STAGES + 4 * NQT + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM: tile t holds S at t*2*BC and dP at t*2*BC + BC (dS, bf16 pairs, over the first BC/2 columns
@@ -465,10 +467,11 @@ struct BwdQCfg {
   static constexpr int COL_DQ = 2 * NQT * BC;
   static constexpr int TMEM_NEED = 2 * NQT * BC + NQT * D;
   static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
-  static constexpr int NWARPS = 4 * NQT + 2;
+  static constexpr int NWARPS = 4 * NQT + 3;
   static constexpr int NTHREADS = NWARPS * 32;
   static constexpr int LOAD_WARP = 4 * NQT;
-  static constexpr int MMA_WARP = 4 * NQT + 1;
+  static constexpr int MMA_WARP = 4 * NQT + 1;   // S, dP (two issuing warps, as in the dK/dV kernel)
+  static constexpr int GRAD_WARP = 4 * NQT + 2;  // dQ
   static constexpr int MAXREG = RegBudget<NWARPS, 1>::VALUE;
   static_assert(D % CHUNK == 0 && BC % 64 == 0 && BC <= 128, "tile");
   static_assert(TMEM_NEED <= 512, "tensor memory");
@@ -552,7 +555,9 @@ __global__ void __maxnreg__(C::MAXREG)
   auto bar_sf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + t); };
   auto bar_pf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + C::NQT + t); };
   auto bar_od = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 2 * C::NQT + t); };
-  const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT);
+  auto bar_gf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT + t); };
+  const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 4 * C::NQT);
+  const uint32_t bar_drain_g = bar_drain + 8u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -568,8 +573,10 @@ __global__ void __maxnreg__(C::MAXREG)
       mbar_init(bar_sf(t), 1);
       mbar_init(bar_pf(t), 4);
       mbar_init(bar_od(t), 1);
+      mbar_init(bar_gf(t), 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_drain_g, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -628,96 +635,89 @@ __global__ void __maxnreg__(C::MAXREG)
         if (nvs > 0) mbar_wait_drain(bar_vf(s), (nvs - 1) & 1, p.err, WB_DRAIN);
       }
     }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    // A phase that already completed is seen by one non-blocking test; only otherwise does the warp
-    // enter the bounded wait.  The MMA queue is short, so time spent here idles the tensor core.
+  } else if (warp == C::MMA_WARP || warp == C::GRAD_WARP) {
+    // ------------------------------------------------------------ MMA issuers (whole warp, elected issue)
     auto wait_all = [&](uint32_t bar, uint32_t parity, int where) {
       if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where)) != 0;
-    };
-    constexpr uint32_t idesc_s = make_idesc(1, C::BR, C::BC, 0, 0);  // S = Q K^T, dP = dO V^T
-    constexpr uint32_t idesc_g = make_idesc(1, C::BR, C::D, 0, 1);   // dQ += dS K (K MN-major)
-    const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-    const uint64_t ddo0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
-    const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-    const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
-    const uint64_t dkm0 = sdesc_sw128(sbase + C::OFF_K, C::KV_CH_BYTES, 1024);
-    auto issue_scores = [&](int t, int s) {
-      const uint32_t col = t * 2 * C::BC;
-      const uint64_t to = static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
-      const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
-      if (elect_one()) {  // one lane issues the whole batch
-#pragma unroll
-        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-          const int e = kk * C::MMA_K;
-          const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-          const int e = kk * C::MMA_K;
-          const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-          mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
-        }
-      }
-      __syncwarp();
-    };
-    auto issue_dq = [&](int t, int s, bool acc) {
-      const uint32_t a_tmem = tmem + t * 2 * C::BC;
-      const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
-          const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-          mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
-                    (acc || kk > 0) ? 1u : 0u);
-        }
-      }
-      __syncwarp();
     };
     auto commit = [&](uint32_t bar) {
       if (elect_one()) mma_commit(bar);
       __syncwarp();
     };
-    bool ok = wait_all(bar_q, 0, WB_Q) && wait_all(bar_kf(0), 0, WB_KF) && wait_all(bar_vf(0), 0, WB_VF);
-    if (ok) {
-      tc_fence_after();
+    if (warp == C::MMA_WARP) {
+      // S_t = Q_t K_j^T and dP_t = dO_t V_j^T once K_j, V_j have landed and dQ_t(j-1) -- the last reader
+      // of dS_t, which sits over S_t -- has completed.
+      constexpr uint32_t idesc_s = make_idesc(1, C::BR, C::BC, 0, 0);
+      const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t ddo0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      bool ok = wait_all(bar_q, 0, WB_Q);
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j % C::STAGES;
+        ok = wait_all(bar_kf(s), (j / C::STAGES) & 1, WB_KF) && wait_all(bar_vf(s), (j / C::STAGES) & 1, WB_VF);
+        for (int t = 0; ok && t < C::NQT; ++t) {
+          if (j > 0) ok = wait_all(bar_gf(t), (j - 1) & 1, WB_PF);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t col = t * 2 * C::BC;
+          const uint64_t to = static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
+          const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+          if (elect_one()) {  // one lane issues the whole batch
 #pragma unroll
-      for (int t = 0; t < C::NQT; ++t) {
-        issue_scores(t, 0);
-        commit(bar_sf(t));
-      }
-      commit(bar_ve(0));
-    }
-    for (int j = 0; ok && j < T; ++j) {
-      const int s = j % C::STAGES;
-      const int j1 = j + 1;
-      const int s1 = j1 % C::STAGES;
-      if (j1 < T) {
-        ok = wait_all(bar_kf(s1), (j1 / C::STAGES) & 1, WB_KF) && wait_all(bar_vf(s1), (j1 / C::STAGES) & 1, WB_VF);
-        if (!ok) break;
-      }
+            for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+              const int e = kk * C::MMA_K;
+              const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+              const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+              mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
+            }
 #pragma unroll
-      for (int t = 0; t < C::NQT; ++t) {
-        ok = wait_all(bar_pf(t), j & 1, WB_PF);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dq(t, s, j > 0);
-        if (t == C::NQT - 1) commit(bar_ke(s));
-        if (j1 < T) {
-          issue_scores(t, s1);
+            for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+              const int e = kk * C::MMA_K;
+              const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+              const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+              mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
+            }
+          }
+          __syncwarp();
           commit(bar_sf(t));
-          if (t == C::NQT - 1) commit(bar_ve(s1));
-        } else {
-          commit(bar_od(t));
         }
+        if (ok) commit(bar_ve(s));  // V_j is read by dP only
       }
+      commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
+    } else {
+      // dQ_t += dS_t K_j once the tile's warpgroup has written dS_t.
+      constexpr uint32_t idesc_g = make_idesc(1, C::BR, C::D, 0, 1);  // K MN-major
+      const uint64_t dkm0 = sdesc_sw128(sbase + C::OFF_K, C::KV_CH_BYTES, 1024);
+      bool ok = true;
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j % C::STAGES;
+        ok = wait_all(bar_kf(s), (j / C::STAGES) & 1, WB_KF);  // complete already: K_j was read by S
+        for (int t = 0; ok && t < C::NQT; ++t) {
+          ok = wait_all(bar_pf(t), j & 1, WB_PF);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + t * 2 * C::BC;
+          const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
+              const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+              mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          __syncwarp();
+          commit(j + 1 < T ? bar_gf(t) : bar_od(t));
+        }
+        // K_j is read by S (complete before its dS existed) and by dQ, complete at this commit
+        if (ok) commit(bar_ke(s));
+      }
+      commit(bar_drain_g);
+      mbar_wait_drain(bar_drain_g, 0, p.err, WB_DRAIN);
     }
-    commit(bar_drain);
-    mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
   } else {
     // ------------------------------------------------------------ elementwise warpgroups: thread = query row
     const int t = warp >> 2;
