@@ -447,6 +447,66 @@ int fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o, i
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Groups of at least this many query heads per key/value head decode on the tensor cores: the group's
+// queries are the rows of a bf16 forward (one 128-row query tile per CTA) over the head's keys, split
+// into the decode's chunks.
+// FA_GQA_TC_MIN_GROUP overrides it in tuning builds.
+#ifndef FA_GQA_TC_MIN_GROUP
+#define FA_GQA_TC_MIN_GROUP 4
+#endif
+constexpr int kGqaTensorMinGroup = FA_GQA_TC_MIN_GROUP;
+
+// Grouped-query decode through the forward kernel in split mode: the G = H / Hkv query heads of a
+// key/value head are contiguous in q, so q is a [B*Hkv, G, d] prefill over that head's keys; chunk s
+// covers keys [s*L, (s+1)*L) with L a whole number of key tiles, and the forward merge combines the
+// chunks in merge_order.  ws holds the fp32 states: O [splits][B*H][d], then (m, l) [splits][B*H].
+cudaError_t gqa_decode_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int Hkv, int Nk, int d, int splits, int L, float scale, char* ws,
+                               const int* merge_order, int* err, cudaStream_t st) {
+  const fa::FwdGeometry geo = fa::fwd_geometry_decode(d);
+  const int G = H / Hkv, BHkv = B * Hkv;
+  CUtensorMap tq, tk, tv;
+  if (encode_map(&tq, q, true, BHkv, G, d, geo.box_cols, geo.q_rows) != FA_OK ||
+      encode_map(&tk, k, true, BHkv, Nk, d, geo.box_cols, geo.kv_rows) != FA_OK ||
+      encode_map(&tv, v, true, BHkv, Nk, d, geo.box_cols, geo.kv_rows) != FA_OK)
+    return cudaErrorInvalidValue;
+  const size_t rows = static_cast<size_t>(B) * H;
+  fa::FwdLaunch a;
+  a.tm_q = &tq;
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.err = err;
+  a.BH = BHkv;
+  a.Nq = G;
+  a.Nk = Nk;
+  a.H = Hkv;
+  a.Hkv = Hkv;
+  a.kv_per_split = L;
+  a.n_split = splits;
+  a.ws_o = splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+  a.ws_ml = splits > 1 ? reinterpret_cast<float*>(ws + round256(static_cast<size_t>(splits) * rows * d * sizeof(float)))
+                       : nullptr;
+  a.causal = 0;
+  a.c = scale * 1.4426950408889634f;
+  a.tau = 8.0f;
+  a.fault = 0;
+  a.stream = st;
+  cudaError_t e = (d == 64) ? fa::launch_fwd_decode_d64(a) : fa::launch_fwd_decode_d128(a);
+  if (e == cudaSuccess && splits > 1)
+    e = fa::launch_fwd_merge(a.ws_o, a.ws_ml, o, lse, static_cast<long long>(rows), d, splits, 1, st, merge_order);
+  return e;
+}
+
+}  // namespace
+
+extern "C" {
+
 int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int Nk, int d,
                           int splits, float scale, void* workspace, size_t workspace_bytes, const int* merge_order,
                           float* lse, fa_stream_t stream) {
@@ -476,6 +536,18 @@ int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, 
     cudaError_t ea = cudaMallocAsync(&ws, need, st);
     if (ea != cudaSuccess) return cuda_fail(ea);
   }
+  const int L = (Nk + splits - 1) / splits;
+  const int tile = fa::fwd_geometry_decode(d).kv_rows;
+  cudaError_t e;
+  if (H / Hkv >= kGqaTensorMinGroup && L % tile == 0 && static_cast<long long>(splits - 1) * L < Nk) {
+    e = gqa_decode_forward(q, k, v, o, lse, B, H, Hkv, Nk, d, splits, L, scale, static_cast<char*>(ws), merge_order,
+                           err, st);
+    if (workspace == nullptr) {
+      cudaError_t e2 = cudaFreeAsync(ws, st);
+      if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  }
   fa::DecodeGqaLaunch a;
   a.q = q;
   a.k = k;
@@ -493,7 +565,7 @@ int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, 
   a.splits = splits;
   a.c = scale * 1.4426950408889634f;
   a.stream = st;
-  cudaError_t e = fa::launch_decode_gqa(a);
+  e = fa::launch_decode_gqa(a);
   if (workspace == nullptr) {
     cudaError_t e2 = cudaFreeAsync(ws, st);
     if (e == cudaSuccess) e = e2;

@@ -1,0 +1,28 @@
+// fa_fwd_decode.cu -- instantiations of the fused forward kernel shaped for grouped-query decode.
+//
+// A grouped-query decode step is a forward with the group's G query heads as the query rows of one
+// 128-row tile (G <= 128 real rows) over one key/value head's keys, split into chunks and merged
+// ("CS349E 第 11 讲 01_online_softmax.py", demo 2: split-KV states and their merge).  With so few
+// real rows the work per key is small, so these configurations keep one query tile per CTA and
+// more CTAs per SM than the prefill ones, to have enough K/V copies in flight:
+//   d = 64 : Bc = 64, one query tile, 3-stage K/V ring (64 KB shared), 3 CTAs/SM
+//   d = 128: Bc = 64, one query tile, 2-stage K/V ring (96 KB shared), 2 CTAs/SM
+#include <cuda_bf16.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+using CfgDecD64 = FwdCfg<__nv_bfloat16, 64, 64, 1, 3, 3, 1>;
+using CfgDecD128 = FwdCfg<__nv_bfloat16, 128, 64, 1, 2, 2, 1>;
+
+cudaError_t launch_fwd_decode_d64(const FwdLaunch& a) { return launch_fwd<CfgDecD64>(a); }
+cudaError_t launch_fwd_decode_d128(const FwdLaunch& a) { return launch_fwd<CfgDecD128>(a); }
+
+FwdGeometry fwd_geometry_decode(int d) {
+  if (d == 64)
+    return FwdGeometry{64, 128, CfgDecD64::BC, 0, CfgDecD64::BR * CfgDecD64::NQT, CfgDecD64::MINB};
+  return FwdGeometry{64, 128, CfgDecD128::BC, 0, CfgDecD128::BR * CfgDecD128::NQT, CfgDecD128::MINB};
+}
+
+}  // namespace fa

@@ -5,9 +5,10 @@
 // associative and commutative, and the closing remarks describe splitting one query's keys
 // over several SMs (flash-decoding) - here applied to every query row of a prefill.
 //
-// One warp per query row: M = max m_s, then l and o accumulate over the splits in index order
-// with weights 2^(m_s - M) (maxima are in log2 units), and O = o / l is written in the output
-// dtype with LSE = (M + log2 l) ln 2.
+// One warp per query row: M = max m_s, then l and o accumulate over the splits in index order (or
+// in a given order: a permutation of the split indices, validated on the device; any other array
+// makes the merge write NaN) with weights 2^(m_s - M) (maxima are in log2 units), and O = o / l is
+// written in the output dtype with LSE = (M + log2 l) ln 2.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -16,12 +17,31 @@
 namespace fa {
 
 constexpr int MERGE_ROWS_PER_CTA = 8;
+constexpr int MERGE_MAX_SPLITS = 4096;
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_CTA)
     fa_fwd_merge_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, void* __restrict__ o,
-                        float* __restrict__ lse, long long rows, int n_split) {
+                        float* __restrict__ lse, long long rows, int n_split, const int* __restrict__ order) {
   constexpr int PER = D / 32;
+  __shared__ unsigned seen[MERGE_MAX_SPLITS / 32];
+  __shared__ int bad;
+  if (order != nullptr) {  // the order must be a permutation of 0 .. n_split - 1
+    for (int i = threadIdx.x; i < (n_split + 31) / 32; i += blockDim.x) seen[i] = 0u;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_split; i += blockDim.x) {
+      const int c = order[i];
+      if (c < 0 || c >= n_split) {
+        bad = 1;
+      } else {
+        const unsigned bit = 1u << (c & 31);
+        if (atomicOr(&seen[c >> 5], bit) & bit) bad = 1;
+      }
+    }
+    __syncthreads();
+  }
+  const bool invalid = order != nullptr && bad;
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * MERGE_ROWS_PER_CTA + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -33,7 +53,8 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_CTA)
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int sp = 0; sp < n_split; ++sp) {
+  for (int i = 0; i < n_split; ++i) {
+    const int sp = order == nullptr ? i : (invalid ? 0 : order[i]);
     const float2 ml = ws_ml[sp * rows + row];
     const float w = ex2_approx(ml.x - M);
     L = fmaf(ml.y, w, L);
@@ -41,7 +62,7 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_CTA)
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = fmaf(src[lane + 32 * e], w, acc[e]);
   }
-  const float inv = 1.f / L;
+  const float inv = invalid ? __int_as_float(0x7fc00000) : 1.f / L;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
     if constexpr (BF16)
@@ -49,19 +70,19 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_CTA)
     else
       static_cast<float*>(o)[row * D + lane + 32 * e] = acc[e] * inv;
   }
-  if (lse != nullptr && lane == 0) lse[row] = (M + log2f(L)) * 0.6931471805599453f;
+  if (lse != nullptr && lane == 0) lse[row] = invalid ? __int_as_float(0x7fc00000) : (M + log2f(L)) * 0.6931471805599453f;
 }
 
 cudaError_t launch_fwd_merge(const float* ws_o, const float* ws_ml, void* o, float* lse, long long rows, int d,
-                             int n_split, int out_bf16, cudaStream_t stream) {
+                             int n_split, int out_bf16, cudaStream_t stream, const int* order) {
   const long long grid = (rows + MERGE_ROWS_PER_CTA - 1) / MERGE_ROWS_PER_CTA;
-  if (grid <= 0 || grid > 0x7FFFFFFFLL || n_split < 1) return cudaErrorInvalidValue;
+  if (grid <= 0 || grid > 0x7FFFFFFFLL || n_split < 1 || n_split > MERGE_MAX_SPLITS) return cudaErrorInvalidValue;
   const dim3 g(static_cast<unsigned>(grid)), b(32 * MERGE_ROWS_PER_CTA);
   const float2* ml = reinterpret_cast<const float2*>(ws_ml);
-  if (d == 64 && out_bf16) fa_fwd_merge_kernel<64, true><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split);
-  else if (d == 64) fa_fwd_merge_kernel<64, false><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split);
-  else if (out_bf16) fa_fwd_merge_kernel<128, true><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split);
-  else fa_fwd_merge_kernel<128, false><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split);
+  if (d == 64 && out_bf16) fa_fwd_merge_kernel<64, true><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
+  else if (d == 64) fa_fwd_merge_kernel<64, false><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
+  else if (out_bf16) fa_fwd_merge_kernel<128, true><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
+  else fa_fwd_merge_kernel<128, false><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
   return cudaGetLastError();
 }
 

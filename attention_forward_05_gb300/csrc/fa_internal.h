@@ -42,8 +42,9 @@ FwdGeometry fwd_geometry_bf16(int d);
 
 // Merge of per-split partial states into O (dtype of the forward) and LSE:
 // O = sum_s o_s 2^(m_s - M) / sum_s l_s 2^(m_s - M), M = max_s m_s; LSE = (M + log2 L) ln 2.
+// `order`: nullptr (index order) or a device int32 permutation of 0 .. n_split - 1.
 cudaError_t launch_fwd_merge(const float* ws_o, const float* ws_ml, void* o, float* lse, long long rows, int d,
-                             int n_split, int out_bf16, cudaStream_t stream);
+                             int n_split, int out_bf16, cudaStream_t stream, const int* order = nullptr);
 
 // fp32 prep pass: qr = tf32(q), kr = tf32(k) (round to nearest), and the key-major copy
 // vt[bh][c][j] = tf32(v[bh][j][c]) for j < Nk, 0 for Nk <= j < Nk_pad.
@@ -53,6 +54,10 @@ cudaError_t launch_fwd_bf16_d64(const FwdLaunch& a);
 cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a);
 cudaError_t launch_fwd_fp32_d64(const FwdLaunch& a);
 cudaError_t launch_fwd_fp32_d128(const FwdLaunch& a);
+// bf16 forward shaped for grouped-query decode (one query tile per CTA); see fa_fwd_decode.cu
+cudaError_t launch_fwd_decode_d64(const FwdLaunch& a);
+cudaError_t launch_fwd_decode_d128(const FwdLaunch& a);
+FwdGeometry fwd_geometry_decode(int d);
 
 struct BwdLaunch {
   // maps for the dK/dV kernel: K, V boxes (64 cols, kv_keys rows); Q, dO boxes (64 cols, kv_qrows rows)

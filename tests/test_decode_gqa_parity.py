@@ -68,3 +68,36 @@ def test_decode_gqa_full_size(cuda_device):
     qq = q.reshape(B * H, d)[heads][:, None]
     check_decode(qq, kk, vv, o.reshape(B * H, d)[heads][:, None], lse.reshape(B * H)[heads][:, None],
                  1 / math.sqrt(d), splits, order, name="decode gqa full size (sampled heads)")
+
+
+def test_decode_gqa_tensor_core_path_full_size(cuda_device):
+    """Groups of 8 (32 query heads on 4 key/value heads) with chunks of whole key tiles go through the
+    forward kernel in split mode: B=32, Nk=32768, d=64, 16 splits, sampled heads against the oracle."""
+    B, H, Hkv, Nk, d, splits = 32, 32, 4, 32768, 64, 16
+    q, _, _ = make_qkv(B, H, 1, 1, d, "bf16", seed=2500, device=cuda_device)
+    _, k, v = make_qkv(B, Hkv, 1, Nk, d, "bf16", seed=2501, device=cuda_device)
+    order = merge_order(splits, 2005)
+    o, lse = fa.fa_decode_splitkv_gqa(q, k, v, splits, with_lse=True,
+                                      merge_order=torch.as_tensor(order, device=cuda_device))
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    rng = np.random.default_rng(2502)
+    heads = sorted({0, B * H - 1, *rng.choice(B * H, 30, replace=False).tolist()})
+    g = H // Hkv
+    kk = torch.stack([k[h // H, (h % H) // g] for h in heads])[:, None]
+    vv = torch.stack([v[h // H, (h % H) // g] for h in heads])[:, None]
+    qq = q.reshape(B * H, d)[heads][:, None]
+    check_decode(qq, kk, vv, o.reshape(B * H, d)[heads][:, None], lse.reshape(B * H)[heads][:, None],
+                 1 / math.sqrt(d), splits, order, name="decode gqa groups of 8, tensor-core path (sampled heads)")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_gqa_bad_merge_order_gives_nan(cuda_device, d):
+    """A merge order that is not a permutation makes both paths write NaN rather than read out of range."""
+    for H, Hkv in ((8, 2), (16, 1)):  # groups of 4 (CUDA cores) and 16 (tensor cores)
+        q, _, _ = make_qkv(1, H, 1, 1, d, "bf16", seed=2600, device=cuda_device)
+        _, k, v = make_qkv(1, Hkv, 1, 1024, d, "bf16", seed=2601, device=cuda_device)
+        bad = torch.tensor([0, 0, 1, 2], dtype=torch.int32, device=cuda_device)
+        o, lse = fa.fa_decode_splitkv_gqa(q, k, v, 4, with_lse=True, merge_order=bad)
+        torch.cuda.synchronize()
+        assert torch.isnan(o.float()).all() and torch.isnan(lse).all()
