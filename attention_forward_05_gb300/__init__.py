@@ -10,6 +10,9 @@ Entry points (same names as the C ABI):
   fa_fwd(q, k, v, scale=None, o=None, lse=None, with_lse=True, kv_splits=0, causal=False, workspace=None)
       -> (o, lse)      (calls fa_fwd_ex; k/v may have fewer heads than q)
   fa_fwd_workspace_bytes(B, H, Hkv, Nq, Nk, d, dtype, causal, kv_splits)
+  fa_fwd_host(q, k, v, scale=None, o=None, lse=None, with_lse=True, causal=False, workspace=None)
+      -> (o, lse)      (host tensors in and out; copies overlap compute)
+  fa_fwd_host_workspace_bytes(B, H, Hkv, Nq, Nk, d, dtype, causal)
   fa_decode_splitkv(q, k, v, splits, o=None) -> o
   fa_decode_splitkv_ex(q, k, v, splits, scale=None, workspace=None, merge_order=None, with_lse=False)
   fa_decode_workspace_bytes(B, H, d, splits)
@@ -72,6 +75,10 @@ def lib() -> ctypes.CDLL:
             L.fa_decode_splitkv_gqa.restype = i
             L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
             L.fa_decode_workspace_bytes.restype = sz
+            L.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
+            L.fa_fwd_host.restype = i
+            L.fa_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+            L.fa_fwd_host_workspace_bytes.restype = sz
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, sz, vp]
             L.fa_bwd.restype = i
             L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
@@ -167,6 +174,58 @@ def fa_fwd_workspace_bytes(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int, d
                            causal: bool = False, kv_splits: int = 0) -> int:
     code = FA_BF16 if dtype == torch.bfloat16 else FA_FP32
     return int(lib().fa_fwd_workspace_bytes(B, H, Hkv, Nq, Nk, d, code, int(bool(causal)), int(kv_splits)))
+
+
+def _need_host_contig(name: str, t: torch.Tensor) -> None:
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fa_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+                o: torch.Tensor | None = None, lse: torch.Tensor | None = None, with_lse: bool = True,
+                causal: bool = False, workspace: torch.Tensor | None = None, stream=None):
+    """fa_fwd on host (CPU) tensors; returns host (o, lse or None), valid once `stream` (default: the
+    current CUDA stream) has finished.  Pinned inputs and outputs let the copies overlap the compute."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need_host_contig(n, t)
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d], k/v [B,Hkv,Nk,d] expected")
+    if q.shape[1] % k.shape[1] != 0:
+        raise ValueError("query heads must be a multiple of key/value heads")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    _need_host_contig("o", o)
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must match q")
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=q.is_pinned())
+    if lse is not None:
+        _need_host_contig("lse", lse)
+        if lse.shape != (B, H, Nq) or lse.dtype != torch.float32:
+            raise ValueError("lse must be fp32 [B,H,Nq]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _need_cuda_contig("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, B, H, Hkv, Nq, Nk, d, float(scale),
+                           _dtype_code(q), int(bool(causal)), ws_ptr, ws_bytes, _stream_handle(stream))
+    _check(st, "fa_fwd_host")
+    return o, lse
+
+
+def fa_fwd_host_workspace_bytes(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int, dtype=torch.bfloat16,
+                                causal: bool = False) -> int:
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_FP32
+    return int(lib().fa_fwd_host_workspace_bytes(B, H, Hkv, Nq, Nk, d, code, int(bool(causal))))
 
 
 def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,

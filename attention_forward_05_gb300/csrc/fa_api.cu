@@ -289,6 +289,154 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Per-device copy streams and events for fa_fwd_host, created on first use.  The mutex keeps one
+// host thread's enqueue sequence (which re-records the shared events) whole.
+constexpr int kHostMaxChunks = 16;
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[kHostMaxChunks] = {}, ev_done[kHostMaxChunks] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.ev_start, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.ev_end, cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e);
+    for (int i = 0; i < kHostMaxChunks; ++i)
+      if ((e = cudaEventCreateWithFlags(&hp.ev_in[i], cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&hp.ev_done[i], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e);
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FA_OK;
+}
+
+// Device layout of fa_fwd_host's workspace: q, k, v, o, lse, each 256-byte aligned.
+struct HostLayout {
+  size_t q = 0, k = 0, v = 0, o = 0, lse = 0, total = 0;
+};
+HostLayout host_layout(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype) {
+  const size_t esz = dtype == FA_BF16 ? 2 : 4;
+  const size_t nq = static_cast<size_t>(B) * H * Nq * d * esz, nkv = static_cast<size_t>(B) * Hkv * Nk * d * esz;
+  HostLayout l;
+  l.q = 0;
+  l.k = l.q + round256(nq);
+  l.v = l.k + round256(nkv);
+  l.o = l.v + round256(nkv);
+  l.lse = l.o + round256(nq);
+  l.total = l.lse + round256(static_cast<size_t>(B) * H * Nq * sizeof(float));
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype, int causal) {
+  FwdPlan pl;
+  if (plan_fwd(B, H, Hkv, Nq, Nk, d, dtype, causal, 1, 0, &pl) != FA_OK) return 0;
+  return host_layout(B, H, Hkv, Nq, Nk, d, dtype).total;
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
+                int Nk, int d, float scale, int dtype, int causal, void* workspace, size_t workspace_bytes,
+                fa_stream_t stream) {
+  if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+  if (workspace && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  FwdPlan pl;
+  int rc = plan_fwd(B, H, Hkv, Nq, Nk, d, dtype, causal, 1, 0, &pl);
+  if (rc != FA_OK) return rc;
+  const HostLayout lay = host_layout(B, H, Hkv, Nq, Nk, d, dtype);
+  if (workspace && workspace_bytes < lay.total) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  int* err = nullptr;
+  if ((rc = device_setup(&dev, &err)) != FA_OK) return rc;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  bool own_ws = false;
+  if (ws == nullptr) {
+    void* wp = nullptr;
+    cudaError_t ea = cudaMallocAsync(&wp, lay.total, st);
+    if (ea != cudaSuccess) return cuda_fail(ea);
+    ws = static_cast<char*>(wp);
+    own_ws = true;
+  }
+  HostPipe* hp = nullptr;
+  std::lock_guard<std::mutex> lk(g_pipe[dev].mu);
+  if ((rc = host_pipe(dev, &hp)) != FA_OK) {
+    if (own_ws) cudaFreeAsync(ws, st);
+    return rc;
+  }
+  // Chunks of whole key/value heads (each with its H / Hkv query heads): q, k, v, o and lse of a chunk
+  // are contiguous ranges.  About 16 MB of input per chunk, at most kHostMaxChunks: the first chunk's
+  // copy in and the last chunk's copy out are the parts that nothing overlaps.
+  const size_t esz = dtype == FA_BF16 ? 2 : 4;
+  const int G = H / Hkv;
+  const long long units = static_cast<long long>(B) * Hkv;
+  const size_t q_unit = static_cast<size_t>(G) * Nq * d * esz, kv_unit = static_cast<size_t>(Nk) * d * esz;
+  const size_t in_bytes = static_cast<size_t>(units) * (q_unit + 2 * kv_unit);
+  long long n = static_cast<long long>((in_bytes + (16u << 20) - 1) / (16u << 20));
+  if (n > kHostMaxChunks) n = kHostMaxChunks;
+  if (n > units) n = units;
+  if (n < 1) n = 1;
+  cudaError_t e = cudaEventRecord(hp->ev_start, st);  // device buffers may still be in use by earlier work
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->s_in, hp->ev_start, 0);
+  int status = FA_OK;
+  for (long long c = 0; c < n && e == cudaSuccess && status == FA_OK; ++c) {
+    const long long u0 = units * c / n, u1 = units * (c + 1) / n;
+    const size_t nu = static_cast<size_t>(u1 - u0);
+    char* dq = ws + lay.q + u0 * q_unit;
+    char* dk = ws + lay.k + u0 * kv_unit;
+    char* dv = ws + lay.v + u0 * kv_unit;
+    char* dout = ws + lay.o + u0 * q_unit;
+    float* dl = reinterpret_cast<float*>(ws + lay.lse) + u0 * G * Nq;
+    if ((e = cudaMemcpyAsync(dq, static_cast<const char*>(q) + u0 * q_unit, nu * q_unit, cudaMemcpyHostToDevice,
+                             hp->s_in)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dk, static_cast<const char*>(k) + u0 * kv_unit, nu * kv_unit, cudaMemcpyHostToDevice,
+                             hp->s_in)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dv, static_cast<const char*>(v) + u0 * kv_unit, nu * kv_unit, cudaMemcpyHostToDevice,
+                             hp->s_in)) != cudaSuccess ||
+        (e = cudaEventRecord(hp->ev_in[c], hp->s_in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, hp->ev_in[c], 0)) != cudaSuccess)
+      break;
+    status = fa_fwd_ex(dq, dk, dv, dout, dl, 1, static_cast<int>(nu) * G, static_cast<int>(nu), Nq, Nk, d, scale,
+                       dtype, causal, 0, nullptr, 0, stream);
+    if (status != FA_OK) break;
+    if ((e = cudaEventRecord(hp->ev_done[c], st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->s_out, hp->ev_done[c], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(static_cast<char*>(o) + u0 * q_unit, dout, nu * q_unit, cudaMemcpyDeviceToHost,
+                             hp->s_out)) != cudaSuccess)
+      break;
+    if (lse && (e = cudaMemcpyAsync(lse + u0 * G * Nq, dl, nu * G * Nq * sizeof(float), cudaMemcpyDeviceToHost,
+                                    hp->s_out)) != cudaSuccess)
+      break;
+  }
+  // the caller's stream waits for the last copy out; later work on it sees finished host buffers
+  cudaError_t e2 = cudaEventRecord(hp->ev_end, hp->s_out);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, hp->ev_end, 0);
+  if (e == cudaSuccess) e = e2;
+  if (own_ws) {
+    e2 = cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (status != FA_OK) return status;
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
            float scale, int dtype, fa_stream_t stream) {
   return fa_fwd_ex(q, k, v, o, lse, B, H, H, Nq, Nk, d, scale, dtype, 0, 0, nullptr, 0, stream);

@@ -105,6 +105,31 @@ size_t fa_fwd_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int 
                               int causal, int kv_splits);
 
 /*
+ * fa_fwd_host -- fa_fwd_ex (kv_splits = 0) on HOST-resident tensors: the library
+ * copies q, k, v to the device, computes, and copies o and lse back, in chunks
+ * of whole key/value heads so that the copies of one chunk overlap the compute of
+ * the previous one (copy-in and copy-out on two internal streams, compute on
+ * `stream`, ordered by events).  The exact attention computed is fa_fwd_ex's.
+ *   q, k, v, o, lse   HOST pointers, same shapes and dtypes as fa_fwd_ex; lse may
+ *                     be NULL.  Page-locked (pinned) memory is needed for the
+ *                     copies to overlap; pageable memory works but serialises.
+ *   workspace         device buffer of at least fa_fwd_host_workspace_bytes(...)
+ *                     bytes (16-byte aligned) that receives the device copies, or
+ *                     NULL to allocate it stream-ordered on `stream`.
+ * Asynchronous: o and lse hold the result once `stream` has completed the work
+ * enqueued up to this call (the call makes `stream` wait for the last copy out).
+ * Calls on one device are serialised on the host while they enqueue.  Returns
+ * FA_OK or an fa_status code.
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int dtype,
+                int causal, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Bytes of device workspace fa_fwd_host needs (0 for invalid arguments). */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype,
+                                   int causal);
+
+/*
  * fa_bwd -- gradients of exact attention (bf16 operands, fp32 accumulation).
  * Given the forward's inputs, its output O and natural-log LSE, and dO (the
  * gradient of a loss with respect to O), writes

@@ -236,3 +236,27 @@ def _dec_gqa(**kw):
 ])
 def test_decode_gqa_rejects(kw, status):
     assert _dec_gqa(**kw) == status
+
+
+def test_fwd_host_rejects_and_workspace():
+    L = fa.lib()
+    # argument errors come back before any device work
+    assert L.fa_fwd_host(None, P, P, P2, None, 1, 4, 2, 64, 64, 64, 0.125, fa.FA_BF16, 0, None, 0, None) == \
+        fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_host(P, P, P, P2, None, 1, 4, 3, 64, 64, 64, 0.125, fa.FA_BF16, 0, None, 0, None) == \
+        fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_host(P, P, P, P2, None, 1, 4, 2, 64, 64, 96, 0.125, fa.FA_BF16, 0, None, 0, None) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert L.fa_fwd_host(P, P, P, P2, None, 1, 4, 2, 64, 64, 64, 0.125, fa.FA_BF16, 0, P, 16, None) == \
+        fa.FA_ERR_INVALID_ARG
+    # q 1*4*100*64*2 = 51200, k/v 1*2*256*64*2 = 65536 each, o 51200, lse 1600 -> 1792 (256-rounded)
+    assert L.fa_fwd_host_workspace_bytes(1, 4, 2, 100, 256, 64, fa.FA_BF16, 0) == 51200 + 65536 * 2 + 51200 + 1792
+    assert L.fa_fwd_host_workspace_bytes(1, 4, 3, 100, 256, 64, fa.FA_BF16, 0) == 0
+
+
+def test_binding_fwd_host_rejects_device_tensors():
+    import torch
+    if not torch.cuda.is_available():
+        x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+        with pytest.raises(TypeError):
+            fa.fa_fwd_host(x, x, x.float())

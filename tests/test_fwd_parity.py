@@ -173,3 +173,23 @@ def test_full_size_sampled(cuda_device, name):
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     rows = sample_rows(w.Nq, 48, seed=w.seed)
     check_fwd(q, k, v, o, lse, w.scale, rows=rows, name=w.name)
+
+
+@pytest.mark.parametrize("dtype,causal,hkv", [("bf16", False, 16), ("bf16", True, 4), ("fp32", False, 16)])
+def test_fwd_host_buffers(cuda_device, dtype, causal, hkv):
+    """fa_fwd_host on pinned host tensors (chunked copies overlapping compute) gives the device result."""
+    B, H, N, d = 2, 16, 1024, 64
+    q, _, _ = make_qkv(B, H, N, 1, d, dtype, seed=3100)
+    _, k, v = make_qkv(B, hkv, 1, N, d, dtype, seed=3101)
+    hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+    o, lse = fa.fa_fwd_host(hq, hk, hv, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    assert not o.is_cuda and o.is_pinned()
+    od, ld = fa.fa_fwd(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device), causal=causal)
+    torch.cuda.synchronize()
+    tol = 2e-2 if dtype == "bf16" else 2e-3
+    assert (o.float() - od.float().cpu()).abs().max().item() <= tol
+    assert (lse - ld.cpu()).abs().max().item() <= 1e-3
+    rows = sample_rows(N, 24, 3102)
+    check_fwd(q, k, v, o, lse, 1 / math.sqrt(d), rows=rows, name=f"fwd_host {dtype} causal={causal}", causal=causal)
