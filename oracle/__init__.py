@@ -23,6 +23,7 @@ and their merge follow [T3] demo 2.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -41,56 +42,84 @@ _dp = ctypes.POINTER(ctypes.c_double)
 _ip = ctypes.POINTER(ctypes.c_int)
 
 
-def build(force: bool = False) -> str:
-    """Compile oracle.c into a shared library with gcc; returns its path.
+def compile_c(src: str, out: str) -> str:
+    """gcc build of a copy of the oracle's C source into a shared library at `out`.
 
     ``-ffp-contract=off`` keeps gcc from fusing multiply-adds (its default on
     aarch64), so the oracle rounds the same way on every host.
     """
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library with gcc; returns its path."""
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
         return _SO
     os.makedirs(_OUT_DIR, exist_ok=True)
-    tmp = _SO + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-           "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _SO)
-    return _SO
+    return compile_c(_SRC, _SO)
+
+
+def source_path() -> str:
+    return _SRC
+
+
+@contextlib.contextmanager
+def swapped_library(path: str):
+    """Test support: the wrappers below call into the library at `path` (another build of oracle.c,
+    e.g. one with a planted mistake) until the block exits."""
+    global _lib
+    other = _configure(ctypes.CDLL(path))
+    with _lock:
+        prev, _lib = _lib, other
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = prev
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            lib.fao_attention_head.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long,
-                                               ctypes.c_long, ctypes.c_long, ctypes.c_double]
-            lib.fao_attention_head.restype = ctypes.c_int
-            lib.fao_attention.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
-                                          ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double]
-            lib.fao_attention.restype = ctypes.c_int
-            lib.fao_attention_head_limits.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
-                                                      ctypes.c_long, ctypes.c_double,
-                                                      ctypes.POINTER(ctypes.c_long)]
-            lib.fao_attention_head_limits.restype = ctypes.c_int
-            lib.fao_attention_bwd_head.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
-                                                   ctypes.c_long, ctypes.c_long, ctypes.c_double]
-            lib.fao_attention_bwd_head.restype = ctypes.c_int
-            lib.fao_attention_bwd_head_limits.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
-                                                          ctypes.c_long, ctypes.c_long, ctypes.c_double,
-                                                          ctypes.POINTER(ctypes.c_long)]
-            lib.fao_attention_bwd_head_limits.restype = ctypes.c_int
-            lib.fao_partial_state.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
-                                              ctypes.c_double, _dp, _dp, _dp]
-            lib.fao_partial_state.restype = ctypes.c_int
-            lib.fao_merge_states.argtypes = [ctypes.c_double, ctypes.c_double, _dp, ctypes.c_double,
-                                             ctypes.c_double, _dp, ctypes.c_long, _dp, _dp, _dp]
-            lib.fao_merge_states.restype = None
-            lib.fao_decode_splitkv.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
-                                               ctypes.c_long, ctypes.c_long, ctypes.c_double, _ip]
-            lib.fao_decode_splitkv.restype = ctypes.c_int
-            _lib = lib
+            _lib = _configure(ctypes.CDLL(build()))
     return _lib
+
+
+def _configure(lib):
+    """Declares the C signatures on a loaded oracle library."""
+    lib.fao_attention_head.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long,
+                                       ctypes.c_long, ctypes.c_long, ctypes.c_double]
+    lib.fao_attention_head.restype = ctypes.c_int
+    lib.fao_attention.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                  ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double]
+    lib.fao_attention.restype = ctypes.c_int
+    lib.fao_attention_head_limits.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                              ctypes.c_long, ctypes.c_double,
+                                              ctypes.POINTER(ctypes.c_long)]
+    lib.fao_attention_head_limits.restype = ctypes.c_int
+    lib.fao_attention_bwd_head.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
+                                           ctypes.c_long, ctypes.c_long, ctypes.c_double]
+    lib.fao_attention_bwd_head.restype = ctypes.c_int
+    lib.fao_attention_bwd_head_limits.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_long,
+                                                  ctypes.c_long, ctypes.c_long, ctypes.c_double,
+                                                  ctypes.POINTER(ctypes.c_long)]
+    lib.fao_attention_bwd_head_limits.restype = ctypes.c_int
+    lib.fao_partial_state.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                      ctypes.c_double, _dp, _dp, _dp]
+    lib.fao_partial_state.restype = ctypes.c_int
+    lib.fao_merge_states.argtypes = [ctypes.c_double, ctypes.c_double, _dp, ctypes.c_double,
+                                     ctypes.c_double, _dp, ctypes.c_long, _dp, _dp, _dp]
+    lib.fao_merge_states.restype = None
+    lib.fao_decode_splitkv.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, ctypes.c_long,
+                                       ctypes.c_long, ctypes.c_long, ctypes.c_double, _ip]
+    lib.fao_decode_splitkv.restype = ctypes.c_int
+    return lib
 
 
 def _f64(a) -> np.ndarray:
