@@ -1,6 +1,7 @@
 /*
- * fa.h -- C ABI of libfa: fused FlashAttention forward and split-KV decode
- * for one NVIDIA GB300 GPU (sm_103a).
+ * fa.h -- C ABI of libfa: fused FlashAttention forward (plain, causal,
+ * grouped-query, split-KV), its backward, and split-KV decode (per-head and
+ * grouped-query) for one NVIDIA GB300 GPU (sm_103a).
  *
  * Sources (web pages, cited by title and section):
  *   [T1] "FlashAttention 简化版：Tiling + Online Softmax" (forceinjection.github.io)
@@ -10,7 +11,8 @@
  * Conventions shared by every entry point
  *   - Tensors are contiguous row-major [B, H, N, d] (d fastest).  Decode q and
  *     o are [B, H, d] (one query per head).  LSE is fp32 [B, H, Nq].
- *   - Every pointer is a DEVICE pointer owned by the caller; base addresses
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller (except the
+ *     tensors of fa_fwd_host, which are host pointers); device base addresses
  *     must be 16-byte aligned.  The library never frees caller memory and
  *     keeps no pointer after a call returns.
  *   - Calls are asynchronous: they validate, enqueue kernels on `stream`
