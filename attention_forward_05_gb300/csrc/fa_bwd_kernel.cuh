@@ -60,6 +60,23 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Warp-collective load of 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Warp-collective store of 8 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 template <int NWARPS, int MINB>
 struct RegBudget {  // registers per thread: 16384 per SM sub-partition, shared by ceil(warps/4) warps
   static constexpr int PER_SUB = (NWARPS * MINB + 3) / 4;
@@ -137,20 +154,29 @@ struct BwdKVParams {
 // (-L log2 e, -D) by column pairs.  MASK: columns q < qmin are above the causal diagonal (P = 0).
 template <class C, bool MASK>
 __device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, const float4* rv, uint64_t c2, int qmin) {
+  // 16-column chunks: the TMEM loads of chunk cc + 1 are in flight while chunk cc is computed, and
+  // each chunk's 8 packed columns are stored at once (columns 8 cc .. 8 cc + 7, all read already).
+  constexpr int NCHK = C::BQ / 16;
+  uint32_t sr[2][16], dr[2][16];
+  tmem_ld16(tS, sr[0]);
+  tmem_ld16(tdP, dr[0]);
+  tmem_wait_ld();
+  reg_fence(sr[0]);
+  reg_fence(dr[0]);
 #pragma unroll
-  for (int cc = 0; cc < C::BQ / 32; ++cc) {
-    uint32_t sr[32], dr[32];
-    tmem_ld32(tS + cc * 32, sr);
-    tmem_ld32(tdP + cc * 32, dr);
-    tmem_wait_ld();
-    reg_fence(sr);
-    reg_fence(dr);
-    uint32_t pk_p[16], pk_ds[16];
+  for (int cc = 0; cc < NCHK; ++cc) {
+    if (cc + 1 < NCHK) {
+      tmem_ld16(tS + (cc + 1) * 16, sr[(cc + 1) & 1]);
+      tmem_ld16(tdP + (cc + 1) * 16, dr[(cc + 1) & 1]);
+    }
+    const uint32_t(&s16)[16] = sr[cc & 1];
+    const uint32_t(&d16)[16] = dr[cc & 1];
+    uint32_t pk_p[8], pk_ds[8];
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const int q = cc * 32 + e;
+    for (int e = 0; e < 16; e += 2) {
+      const int q = cc * 16 + e;
       const float4 vv = rv[q / 2];  // (-L log2 e, -D) of columns q and q + 1
-      const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(s16[e]), __uint_as_float(s16[e + 1])), c2,
                                 f2_pack(vv.x, vv.y));
       float x0, x1;
       f2_unpack_f(x, x0, x1);
@@ -159,16 +185,20 @@ __device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, cons
         if (q < qmin) p0 = 0.f;
         if (q + 1 < qmin) p1 = 0.f;
       }
-      const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), f2_pack(vv.z, vv.w));
+      const uint64_t t = f2_add(f2_pack(__uint_as_float(d16[e]), __uint_as_float(d16[e + 1])), f2_pack(vv.z, vv.w));
       const uint64_t ds = f2_mul(f2_pack(p0, p1), t);
       float ds0, ds1;
       f2_unpack_f(ds, ds0, ds1);
       pk_p[e / 2] = pack_bf16x2(p0, p1);
       pk_ds[e / 2] = pack_bf16x2(ds0, ds1);
     }
-    // chunk cc's packed values go to columns 16 cc .. 16 cc + 15, all read already
-    tmem_st16(tS + cc * 16, pk_p);
-    tmem_st16(tdP + cc * 16, pk_ds);
+    tmem_st8(tS + cc * 8, pk_p);
+    tmem_st8(tdP + cc * 8, pk_ds);
+    if (cc + 1 < NCHK) {
+      tmem_wait_ld();
+      reg_fence(sr[(cc + 1) & 1]);
+      reg_fence(dr[(cc + 1) & 1]);
+    }
   }
 }
 
@@ -493,19 +523,28 @@ struct BwdQParams {
 template <class C, bool TAIL>
 __device__ __forceinline__ void dq_elementwise(uint32_t tS, uint32_t tdP, uint64_t c2, uint64_t nl_2, uint64_t nd_2,
                                                int valid) {
-  uint32_t pk[C::BC / 64][32];
+  // 16-column chunks with the next chunk's TMEM loads in flight, as in the dK/dV kernel; chunk cc's
+  // 8 packed dS columns go over S columns 8 cc .. 8 cc + 7, all read already.
+  constexpr int NCHK = C::BC / 16;
+  uint32_t sr[2][16], dr[2][16];
+  tmem_ld16(tS, sr[0]);
+  tmem_ld16(tdP, dr[0]);
+  tmem_wait_ld();
+  reg_fence(sr[0]);
+  reg_fence(dr[0]);
 #pragma unroll
-  for (int cc = 0; cc < C::BC / 32; ++cc) {
-    uint32_t sr[32], dr[32];
-    tmem_ld32(tS + cc * 32, sr);
-    tmem_ld32(tdP + cc * 32, dr);
-    tmem_wait_ld();
-    reg_fence(sr);
-    reg_fence(dr);
+  for (int cc = 0; cc < NCHK; ++cc) {
+    if (cc + 1 < NCHK) {
+      tmem_ld16(tS + (cc + 1) * 16, sr[(cc + 1) & 1]);
+      tmem_ld16(tdP + (cc + 1) * 16, dr[(cc + 1) & 1]);
+    }
+    const uint32_t(&s16)[16] = sr[cc & 1];
+    const uint32_t(&d16)[16] = dr[cc & 1];
+    uint32_t pk[8];
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const int col = cc * 32 + e;
-      const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nl_2);
+    for (int e = 0; e < 16; e += 2) {
+      const int col = cc * 16 + e;
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(s16[e]), __uint_as_float(s16[e + 1])), c2, nl_2);
       float x0, x1;
       f2_unpack_f(x, x0, x1);
       float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -513,16 +552,19 @@ __device__ __forceinline__ void dq_elementwise(uint32_t tS, uint32_t tdP, uint64
         if (col >= valid) p0 = 0.f;
         if (col + 1 >= valid) p1 = 0.f;
       }
-      const uint64_t tt = f2_add(f2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), nd_2);
+      const uint64_t tt = f2_add(f2_pack(__uint_as_float(d16[e]), __uint_as_float(d16[e + 1])), nd_2);
       const uint64_t ds = f2_mul(f2_pack(p0, p1), tt);
       float ds0, ds1;
       f2_unpack_f(ds, ds0, ds1);
-      const int word = col / 2;
-      pk[word / 32][word % 32] = pack_bf16x2(ds0, ds1);
+      pk[e / 2] = pack_bf16x2(ds0, ds1);
+    }
+    tmem_st8(tS + cc * 8, pk);
+    if (cc + 1 < NCHK) {
+      tmem_wait_ld();
+      reg_fence(sr[(cc + 1) & 1]);
+      reg_fence(dr[(cc + 1) & 1]);
     }
   }
-#pragma unroll
-  for (int i = 0; i < C::BC / 64; ++i) tmem_st32(tS + i * 32, pk[i]);
 }
 
 template <class C>
