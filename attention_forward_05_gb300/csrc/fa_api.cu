@@ -529,6 +529,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.causal = causal;
   a.c = scale * 1.4426950408889634f;
   a.scale = scale;
+  a.fault = g_fault.exchange(0);
   a.stream = st;
   cudaError_t e = fa::launch_bwd_bf16(a);
   if (own_ws) {

@@ -91,6 +91,7 @@ cudaError_t launch_dkdv(const BwdLaunch& a) {
   p.causal_off = a.Nk - a.Nq;
   p.c = a.c;
   p.scale = a.scale;
+  p.fault = a.fault;
   if (p.n_qt * C::BQ > a.Nq_pad) return cudaErrorInvalidValue;  // the vectors are read in whole steps
   const long long grid = static_cast<long long>(p.n_kblk) * a.BHkv;
   if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;

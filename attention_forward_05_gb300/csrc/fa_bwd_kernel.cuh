@@ -147,6 +147,7 @@ struct BwdKVParams {
   int causal, causal_off;  // query row i sees keys j <= i + causal_off
   float c;                 // scale * log2(e)
   float scale;
+  int fault;               // test only: 1 = the load warp skips the K/V copy (the waits for it run out)
 };
 
 // One step of a dK/dV elementwise thread (one key row, BQ query columns): P^T = 2^(s c - L log2 e),
@@ -276,11 +277,13 @@ __global__ void __maxnreg__(C::MAXREG)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int n_done = 0;
-      mbar_expect_tx(bar_kv, 2 * C::KV_BYTES);
+      if (p.fault != 1) {
+        mbar_expect_tx(bar_kv, 2 * C::KV_BYTES);
 #pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(sbase + C::OFF_K + c * C::KV_CH_BYTES, &tm_k, bar_kv, c * C::CHUNK, k0, kvbh);
-        tma_load_3d(sbase + C::OFF_V + c * C::KV_CH_BYTES, &tm_v, bar_kv, c * C::CHUNK, k0, kvbh);
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_3d(sbase + C::OFF_K + c * C::KV_CH_BYTES, &tm_k, bar_kv, c * C::CHUNK, k0, kvbh);
+          tma_load_3d(sbase + C::OFF_V + c * C::KV_CH_BYTES, &tm_v, bar_kv, c * C::CHUNK, k0, kvbh);
+        }
       }
       for (int s = 0; s < T; ++s) {
         const int st = s % C::STAGES;
@@ -301,7 +304,7 @@ __global__ void __maxnreg__(C::MAXREG)
         n_done = s + 1;
       }
       // drain every copy issued above before the CTA exits
-      mbar_wait_drain(bar_kv, 0, p.err, WB_DRAIN);
+      if (p.fault != 1) mbar_wait_drain(bar_kv, 0, p.err, WB_DRAIN);
 #pragma unroll
       for (int st = 0; st < C::STAGES; ++st) {
         const int cnt = n_done > st ? (n_done - 1 - st) / C::STAGES + 1 : 0;

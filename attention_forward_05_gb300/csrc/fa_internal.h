@@ -82,6 +82,7 @@ struct BwdLaunch {
   int causal;
   float c;                  // scale * log2(e)
   float scale;
+  int fault;                // test-only fault injection mode for the dK/dV kernel (0 = none)
   cudaStream_t stream;
 };
 

@@ -266,11 +266,12 @@ const char* fa_last_cuda_error_string(void);
 
 /*
  * fa_debug_set_fault -- TEST ONLY.  Arms a host-side fault for the next
- * fa_fwd launch on this process: mode 1 makes the kernel's load warp skip
- * its first key-tile copy (and its expected-byte count), so the consumer's
- * bounded wait runs out, the kernel abandons its work, records
- * FA_ERR_TIMEOUT and returns.  mode 0 disarms.  Returns FA_OK or
- * FA_ERR_INVALID_ARG.
+ * fa_fwd / fa_fwd_ex or fa_bwd call on this process (whichever comes first):
+ * mode 1 makes the load warp of the forward kernel skip its first key-tile
+ * copy, or the load warp of the backward's dK/dV kernel skip its key/value
+ * copy (and the expected-byte count), so the consumers' bounded waits run
+ * out, the kernel abandons its work, records FA_ERR_TIMEOUT and returns.
+ * mode 0 disarms.  Returns FA_OK or FA_ERR_INVALID_ARG.
  */
 int fa_debug_set_fault(int mode);
 

@@ -31,3 +31,26 @@ def test_skipped_copy_times_out_then_recovers(cuda_device, d):
     torch.cuda.synchronize()
     assert fa.fa_check_device_error() == fa.FA_OK
     check_fwd(q, k, v, o, lse, sc, name=f"after fault d{d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_skipped_copy_times_out_then_recovers(cuda_device, d):
+    """The dK/dV kernel's load warp skips its key/value copy: both MMA warps' waits for it run out, the
+    elementwise warps and the loader see the abort flag, and the host reads FA_ERR_TIMEOUT.  The next
+    backward call is correct."""
+    from attention_forward_05_gb300.inputs import make_dout
+    from parity import check_bwd
+    q, k, v = make_qkv(1, 1, 128, 256, d, "bf16", seed=92, device=cuda_device)  # two dK/dV CTAs
+    dout = make_dout(1, 1, 128, d, "bf16", seed=93, device=cuda_device)
+    sc = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd(q, k, v, scale=sc)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    assert fa.fa_debug_set_fault(1) == fa.FA_OK
+    fa.fa_bwd(q, k, v, o, dout, lse, scale=sc)
+    assert fa.fa_check_device_error() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_check_device_error() == fa.FA_OK
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, dout, lse, scale=sc)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, name=f"bwd after fault d{d}")
