@@ -37,7 +37,7 @@
 
 namespace fa {
 
-template <typename T, int D_, int BC_, int NQT_, int STAGES_, int MINB_ = 1, int SPLIT_ = 1>
+template <typename T, int D_, int BC_, int NQT_, int STAGES_, int MINB_ = 1, int SPLIT_ = 1, bool PV2_ = false>
 struct FwdCfg {
   using Elem = T;
   static constexpr int D = D_;
@@ -46,6 +46,9 @@ struct FwdCfg {
   static constexpr int STAGES = STAGES_;
   static constexpr int MINB = MINB_;    // CTAs per SM the launch bounds ask for
   static constexpr int SPLIT = SPLIT_;  // softmax warpgroups per query tile, each owning BC/SPLIT key columns
+  // PV2: the softmax hands over P in two halves (key columns [0, BC/2) first), and P V of the first
+  // half is issued while the second half is still being exponentiated.
+  static constexpr bool PV2 = PV2_;
   static constexpr int BR = 128;
   static constexpr int ESZ = static_cast<int>(sizeof(T));
   static constexpr bool TF32 = (ESZ == 4);
@@ -66,7 +69,7 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT], drain
-  static constexpr int NBAR = 1 + 4 * STAGES + 3 * NQT + 1;
+  static constexpr int NBAR = 1 + 4 * STAGES + 4 * NQT + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
   // exchange of partial row maxima / sums between the SPLIT warpgroups of a tile: [2 slots][NQT][SPLIT][128]
   static constexpr int OFF_XCHG = OFF_MISC + 16;
@@ -96,6 +99,7 @@ struct FwdCfg {
   static_assert(BC % 32 == 0 && BC >= 32 && BC <= 256, "key tile");
   static_assert(COLS % 32 == 0 && PCOLS_W % 32 == 0 && OCOLS % 32 == 0, "split into whole 32-column chunks");
   static_assert(NQT <= 8, "one named barrier per tile");
+  static_assert(!PV2 || (SPLIT == 1 && !TF32 && BC >= 128 && (BC / 2) % 64 == 0), "P handed over in two halves of whole packed chunks");
   static_assert(TMEM_NEED <= 512 / MINB, "tensor memory");
   static_assert(SMEM_BYTES * MINB <= 227 * 1024, "shared memory");
 };
@@ -226,6 +230,7 @@ __global__ void __maxnreg__(C::MAXREG)
   auto bar_pf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + C::NQT + t); };
   auto bar_od = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 2 * C::NQT + t); };
   const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT);
+  auto bar_ph = [&](int t) { return bar0 + 8u * (2 + 4 * C::STAGES + 3 * C::NQT + t); };  // first half of P
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -240,6 +245,7 @@ __global__ void __maxnreg__(C::MAXREG)
     for (int t = 0; t < C::NQT; ++t) {
       mbar_init(bar_sf(t), 1);
       mbar_init(bar_pf(t), 4 * C::SPLIT);  // one arrive per softmax warp of the tile
+      mbar_init(bar_ph(t), 4);
       mbar_init(bar_od(t), 1);
     }
     mbar_init(bar_drain, 1);
@@ -337,12 +343,12 @@ __global__ void __maxnreg__(C::MAXREG)
           if (elect_one()) mma_ss<C::TF32>(d_tmem, qa + oq, kb + ok_, idesc_qk, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int s, bool acc) {
+      auto issue_pv = [&](int t, int s, bool acc, int kk0 = 0, int kk1 = C::BC / C::MMA_K) {
         const uint32_t d_tmem = tmem + C::O_COL0 + t * C::D;
         const uint32_t a_tmem = tmem + t * C::BC;
         const uint64_t vb = dv0 + static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
+        for (int kk = kk0; kk < kk1; ++kk) {
           uint32_t ov;
           if constexpr (C::V_KMAJOR) {  // [D rows][Bc keys]: step along keys inside 128-byte segments
             const int e = kk * C::MMA_K;
@@ -379,10 +385,19 @@ __global__ void __maxnreg__(C::MAXREG)
         if (!ok) break;
 #pragma unroll
         for (int t = 0; t < C::NQT; ++t) {
+          if constexpr (C::PV2) {  // first half of P V as soon as the first half of P is in
+            ok = wait_all(bar_ph(t), j & 1, W_PF);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, s, j > 0, 0, C::BC / C::MMA_K / 2);
+          }
           ok = wait_all(bar_pf(t), j & 1, W_PF);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, s, j > 0);
+          if constexpr (C::PV2)
+            issue_pv(t, s, true, C::BC / C::MMA_K / 2, C::BC / C::MMA_K);
+          else
+            issue_pv(t, s, j > 0);
           if (t == C::NQT - 1) commit(bar_ve(s));
           if (j1 < T) {
             issue_qk(t, s1);
@@ -536,6 +551,43 @@ __global__ void __maxnreg__(C::MAXREG)
         else softmax_p_tf32<C::COLS, true>(sr, c2, negm2, valid, rs2);
 #pragma unroll
         for (int i = 0; i < C::COLS / 32; ++i) tmem_st32(tP + i * 32, sr[i]);
+      } else if constexpr (C::PV2) {
+        // First half of P, then the O correction (P V of this step accumulates into the corrected
+        // O), then the signal for the first half of P V; the second half of P follows.
+        constexpr int HC = C::COLS / 2;
+        uint32_t pk[C::PCOLS_W / 32][32];
+        auto& sr_a = reinterpret_cast<uint32_t(&)[HC / 32][32]>(sr[0]);
+        auto& sr_b = reinterpret_cast<uint32_t(&)[HC / 32][32]>(sr[HC / 32]);
+        auto& pk_a = reinterpret_cast<uint32_t(&)[HC / 64][32]>(pk[0]);
+        auto& pk_b = reinterpret_cast<uint32_t(&)[HC / 64][32]>(pk[HC / 64]);
+        if (valid >= HC) softmax_p_bf16<HC, false>(sr_a, pk_a, c2, negm2, valid, rs2);
+        else softmax_p_bf16<HC, true>(sr_a, pk_a, c2, negm2, valid, rs2);
+#pragma unroll
+        for (int i = 0; i < HC / 64; ++i) tmem_st32(tP + i * 32, pk_a[i]);
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+          for (int cc = 0; cc < C::OCOLS / 32; ++cc) {
+            uint32_t orr[32];
+            tmem_ld32(tO + cc * 32, orr);
+            tmem_wait_ld();
+            reg_fence(orr);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const uint64_t v = f2_mul(f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), a2);
+              f2_unpack(v, orr[e], orr[e + 1]);
+            }
+            tmem_st32(tO + cc * 32, orr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ph(t));
+        if (valid >= C::COLS) softmax_p_bf16<HC, false>(sr_b, pk_b, c2, negm2, valid - HC, rs2);
+        else softmax_p_bf16<HC, true>(sr_b, pk_b, c2, negm2, valid - HC, rs2);
+#pragma unroll
+        for (int i = 0; i < HC / 64; ++i) tmem_st32(tP + (HC / 64 + i) * 32, pk_b[i]);
       } else {
         uint32_t pk[C::PCOLS_W / 32][32];
         if (valid >= C::COLS) softmax_p_bf16<C::COLS, false>(sr, pk, c2, negm2, valid, rs2);
@@ -545,7 +597,8 @@ __global__ void __maxnreg__(C::MAXREG)
       }
       // correction of O_t: its last update (P V of step j-1) completed before S_t of step j did,
       // and P V of step j is not issued before every warpgroup of the tile arrives below
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      // (with PV2 it was applied above, before the first half of P was handed over)
+      if (!C::PV2 && j > 0 && __any_sync(0xffffffffu, need)) {
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < C::OCOLS / 32; ++cc) {
