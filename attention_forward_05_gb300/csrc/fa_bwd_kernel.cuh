@@ -89,13 +89,14 @@ enum : int { WB_KV = 0x21, WB_SF, WB_SE, WB_PF, WB_DONE, WB_Q, WB_KF, WB_VF, WB_
 
 // ------------------------------------------------------------------------------------------ dK, dV
 
-template <int D_, int BQ_, int STAGES_, int NSLOT_>
+template <int D_, int BQ_, int STAGES_, int NSLOT_, bool HALF_ = true>
 struct BwdKVCfg {
   static constexpr int D = D_;
   static constexpr int BK = 128;             // keys per CTA (TMEM lanes, M of every MMA)
   static constexpr int BQ = BQ_;             // query rows per step (N of S^T and dP^T, K of dV and dK)
   static constexpr int STAGES = STAGES_;     // ring of (Q_i, dO_i, row values)
   static constexpr int NSLOT = NSLOT_;       // TMEM slots for (S^T, dP^T); one elementwise warpgroup each
+  static constexpr bool HALF = HALF_;        // gradient MMAs start on the first half of a step's columns
   static constexpr int CHUNK = 64;           // bf16 elements per 128-byte swizzled row segment
   static constexpr int NCH = D / CHUNK;
   static constexpr int MMA_K = 16;
@@ -111,8 +112,8 @@ struct BwdKVCfg {
   static constexpr int OFF_VEC = OFF_DO + STAGES * QS_BYTES;  // stage s at + s * VEC_BYTES
   static constexpr int OFF_BAR = OFF_VEC + STAGES * VEC_BYTES;
   // barriers: kv_full, st_full[S], st_empty[S], s_full[NSLOT], p_full[NSLOT], g_free[NSLOT], done,
-  // drain (score issuer), drain (gradient issuer)
-  static constexpr int NBAR = 1 + 2 * STAGES + 3 * NSLOT + 3;
+  // drain (score issuer), drain (gradient issuer), p_half[NSLOT]
+  static constexpr int NBAR = 1 + 2 * STAGES + 4 * NSLOT + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM: slot b holds S^T at b*2*BQ and dP^T at b*2*BQ + BQ; P^T and dS^T (bf16 pairs) are written
@@ -154,7 +155,8 @@ struct BwdKVParams {
 // dS^T = P^T (dP^T - D), both written back over S^T and dP^T as bf16 pairs.  rv holds the step's
 // (-L log2 e, -D) by column pairs.  MASK: columns q < qmin are above the causal diagonal (P = 0).
 template <class C, bool MASK>
-__device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, const float4* rv, uint64_t c2, int qmin) {
+__device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, const float4* rv, uint64_t c2, int qmin,
+                                                 uint32_t bar_half, int lane) {
   // 16-column chunks: the TMEM loads of chunk cc + 1 are in flight while chunk cc is computed, and
   // each chunk's 8 packed columns are stored at once (columns 8 cc .. 8 cc + 7, all read already).
   constexpr int NCHK = C::BQ / 16;
@@ -195,6 +197,12 @@ __device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, cons
     }
     tmem_st8(tS + cc * 8, pk_p);
     tmem_st8(tdP + cc * 8, pk_ds);
+    if (C::HALF && cc == NCHK / 2 - 1) {  // the first half of the step's query columns is in: the gradient MMAs may start
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_half);
+    }
     if (cc + 1 < NCHK) {
       tmem_wait_ld();
       reg_fence(sr[(cc + 1) & 1]);
@@ -236,6 +244,7 @@ __global__ void __maxnreg__(C::MAXREG)
   const uint32_t bar_done = bar0 + 8u * (1 + 2 * C::STAGES + 3 * C::NSLOT);
   const uint32_t bar_drain = bar_done + 8u;
   const uint32_t bar_drain_g = bar_done + 16u;
+  auto bar_ph = [&](int w) { return bar_done + 24u + 8u * w; };  // first half of P^T, dS^T written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -249,6 +258,7 @@ __global__ void __maxnreg__(C::MAXREG)
       mbar_init(bar_sf(w), 1);
       mbar_init(bar_pf(w), 4);  // one arrive per warp of the warpgroup
       mbar_init(bar_gf(w), 1);
+      mbar_init(bar_ph(w), 4);
     }
     mbar_init(bar_done, 1);
     mbar_init(bar_drain, 1);
@@ -367,28 +377,39 @@ __global__ void __maxnreg__(C::MAXREG)
       const uint64_t dqm0 = sdesc_sw128(sbase + C::OFF_Q, C::QS_CH_BYTES, 1024);   // Q as MN-major B
       const uint64_t ddom0 = sdesc_sw128(sbase + C::OFF_DO, C::QS_CH_BYTES, 1024); // dO as MN-major B
       for (int s = 0; ok && s < T; ++s) {
-        ok = wait_all(bar_full(s % C::STAGES), (s / C::STAGES) & 1, WB_SF);  // complete already
-        ok = ok && wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
-        if (!ok) break;
-        tc_fence_after();
         const int st = s % C::STAGES;
         const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
         const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
-        if (elect_one()) {
+        auto issue = [&](int kk0, int kk1) {
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
-            const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
-            mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
-                      (s > 0 || kk > 0) ? 1u : 0u);
-          }
+            for (int kk = kk0; kk < kk1; ++kk) {
+              const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
+              mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
+                        (s > 0 || kk > 0) ? 1u : 0u);
+            }
 #pragma unroll
-          for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
-            const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-            mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
-                      (s > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = kk0; kk < kk1; ++kk) {
+              const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+              mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
+                        (s > 0 || kk > 0) ? 1u : 0u);
+            }
           }
+          __syncwarp();
+        };
+        ok = wait_all(bar_full(st), (s / C::STAGES) & 1, WB_SF);  // complete already
+        // with HALF, the first half of the query rows as soon as the warpgroup has written it
+        constexpr int KH = C::HALF ? C::BQ / C::MMA_K / 2 : 0;
+        if (C::HALF) {
+          ok = ok && wait_all(bar_ph(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
+          if (!ok) break;
+          tc_fence_after();
+          issue(0, KH);
         }
-        __syncwarp();
+        ok = ok && wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
+        if (!ok) break;
+        tc_fence_after();
+        issue(KH, C::BQ / C::MMA_K);
         commit(bar_gf(s % C::NSLOT));       // the slot may be overwritten
         commit(bar_empty(s % C::STAGES));   // the stage may be refilled (its score MMAs completed earlier)
       }
@@ -420,9 +441,9 @@ __global__ void __maxnreg__(C::MAXREG)
       // causal: query column q (row step_qt(s)*BQ + q) is visible to this key when q >= qmin
       const int qmin = p.causal ? key - p.causal_off - step_qt(s) * C::BQ : 0;
       if (__any_sync(0xffffffffu, qmin > 0))
-        dkdv_elementwise<C, true>(tS, tdP, rv, c2, qmin);
+        dkdv_elementwise<C, true>(tS, tdP, rv, c2, qmin, bar_ph(w), lane);
       else
-        dkdv_elementwise<C, false>(tS, tdP, rv, c2, qmin);
+        dkdv_elementwise<C, false>(tS, tdP, rv, c2, qmin, bar_ph(w), lane);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -471,13 +492,14 @@ __global__ void __maxnreg__(C::MAXREG)
 
 // ------------------------------------------------------------------------------------------ dQ
 
-template <int D_, int BC_, int STAGES_>
+template <int D_, int BC_, int STAGES_, bool HALF_ = true>
 struct BwdQCfg {
   static constexpr int D = D_;
   static constexpr int BR = 128;           // query rows per tile (TMEM lanes)
   static constexpr int NQT = 2;            // query tiles per CTA, alternating between the two warpgroups
   static constexpr int BC = BC_;           // keys per step
   static constexpr int STAGES = STAGES_;   // ring of (K_j, V_j)
+  static constexpr bool HALF = HALF_;      // dQ MMAs start on the first half of a step's keys
   static constexpr int CHUNK = 64;
   static constexpr int NCH = D / CHUNK;
   static constexpr int MMA_K = 16;
@@ -491,8 +513,8 @@ struct BwdQCfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT],
-  // g_free[NQT], drain (score issuer), drain (dQ issuer)
-  static constexpr int NBAR = 1 + 4 * STAGES + 4 * NQT + 2;
+  // g_free[NQT], drain (score issuer), drain (dQ issuer), p_half[NQT]
+  static constexpr int NBAR = 1 + 4 * STAGES + 5 * NQT + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM: tile t holds S at t*2*BC and dP at t*2*BC + BC (dS, bf16 pairs, over the first BC/2 columns
@@ -525,7 +547,7 @@ struct BwdQParams {
 // dS = P (dP - D), written back over S as bf16 pairs.  TAIL: columns >= valid are masked (P = 0).
 template <class C, bool TAIL>
 __device__ __forceinline__ void dq_elementwise(uint32_t tS, uint32_t tdP, uint64_t c2, uint64_t nl_2, uint64_t nd_2,
-                                               int valid) {
+                                               int valid, uint32_t bar_half, int lane) {
   // 16-column chunks with the next chunk's TMEM loads in flight, as in the dK/dV kernel; chunk cc's
   // 8 packed dS columns go over S columns 8 cc .. 8 cc + 7, all read already.
   constexpr int NCHK = C::BC / 16;
@@ -562,6 +584,12 @@ __device__ __forceinline__ void dq_elementwise(uint32_t tS, uint32_t tdP, uint64
       pk[e / 2] = pack_bf16x2(ds0, ds1);
     }
     tmem_st8(tS + cc * 8, pk);
+    if (C::HALF && cc == NCHK / 2 - 1) {  // the first half of the step's keys is in: dQ += dS K may start
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_half);
+    }
     if (cc + 1 < NCHK) {
       tmem_wait_ld();
       reg_fence(sr[(cc + 1) & 1]);
@@ -603,6 +631,7 @@ __global__ void __maxnreg__(C::MAXREG)
   auto bar_gf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT + t); };
   const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 4 * C::NQT);
   const uint32_t bar_drain_g = bar_drain + 8u;
+  auto bar_ph = [&](int t) { return bar_drain + 16u + 8u * t; };  // first half of dS written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -619,6 +648,7 @@ __global__ void __maxnreg__(C::MAXREG)
       mbar_init(bar_pf(t), 4);
       mbar_init(bar_od(t), 1);
       mbar_init(bar_gf(t), 1);
+      mbar_init(bar_ph(t), 4);
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain_g, 1);
@@ -741,20 +771,31 @@ __global__ void __maxnreg__(C::MAXREG)
         const int s = j % C::STAGES;
         ok = wait_all(bar_kf(s), (j / C::STAGES) & 1, WB_KF);  // complete already: K_j was read by S
         for (int t = 0; ok && t < C::NQT; ++t) {
+          const uint32_t a_tmem = tmem + t * 2 * C::BC;
+          const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+          auto issue = [&](int kk0, int kk1) {
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = kk0; kk < kk1; ++kk) {
+                const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+                mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            __syncwarp();
+          };
+          // with HALF, the first half of the keys as soon as the warpgroup has written their dS
+          constexpr int KH = C::HALF ? C::BC / C::MMA_K / 2 : 0;
+          if (C::HALF) {
+            ok = wait_all(bar_ph(t), j & 1, WB_PF);
+            if (!ok) break;
+            tc_fence_after();
+            issue(0, KH);
+          }
           ok = wait_all(bar_pf(t), j & 1, WB_PF);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a_tmem = tmem + t * 2 * C::BC;
-          const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
-              const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-              mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          __syncwarp();
+          issue(KH, C::BC / C::MMA_K);
           commit(j + 1 < T ? bar_gf(t) : bar_od(t));
         }
         // K_j is read by S (complete before its dS existed) and by dQ, complete at this commit
@@ -788,9 +829,9 @@ __global__ void __maxnreg__(C::MAXREG)
       tc_fence_after();
       const int valid = row_lim - j * C::BC;  // key columns of this step the row may see
       if (__all_sync(0xffffffffu, valid >= C::BC))
-        dq_elementwise<C, false>(tS, tdP, c2, nl_2, nd_2, valid);
+        dq_elementwise<C, false>(tS, tdP, c2, nl_2, nd_2, valid, bar_ph(t), lane);
       else
-        dq_elementwise<C, true>(tS, tdP, c2, nl_2, nd_2, valid);
+        dq_elementwise<C, true>(tS, tdP, c2, nl_2, nd_2, valid, bar_ph(t), lane);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
