@@ -4,7 +4,7 @@
 //            (four softmax warpgroups per SM: the d = 64 softmax is as costly as its MMAs)
 //   d = 128: Bc = 128, two query tiles per CTA, 2-stage K/V ring (192 KB shared), 1 CTA/SM; P is handed
 //            to the MMA warp in two halves, so P V of the first 64 keys overlaps the second half's exps
-// Compiler definitions FA_D64_{BC,NQT,STAGES,MINB} / FA_D128_{...} override the
+// Compiler definitions FA_D64_{BC,NQT,STAGES,MINB,SPLIT,PV2} / FA_D128_{...} override the
 // tile configuration for tuning builds.
 #include <cuda_bf16.h>
 
@@ -40,13 +40,17 @@
 #ifndef FA_D128_SPLIT
 #define FA_D128_SPLIT 1
 #endif
+#ifndef FA_D64_PV2
+#define FA_D64_PV2 0
+#endif
 #ifndef FA_D128_PV2
 #define FA_D128_PV2 1
 #endif
 
 namespace fa {
 
-using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, FA_D64_BC, FA_D64_NQT, FA_D64_STAGES, FA_D64_MINB, FA_D64_SPLIT>;
+using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, FA_D64_BC, FA_D64_NQT, FA_D64_STAGES, FA_D64_MINB, FA_D64_SPLIT,
+                          FA_D64_PV2 != 0>;
 using CfgBf16D128 = FwdCfg<__nv_bfloat16, 128, FA_D128_BC, FA_D128_NQT, FA_D128_STAGES, FA_D128_MINB, FA_D128_SPLIT,
                            FA_D128_PV2 != 0>;
 

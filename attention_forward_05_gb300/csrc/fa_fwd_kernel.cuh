@@ -434,6 +434,7 @@ __global__ void __maxnreg__(C::MAXREG)
     float l = 0.f;
     bool ok = true;
     const uint64_t c2 = f2_pack(c, c);
+    const float p_lim = exp2f(p.tau);  // largest row sum of P that proves no maximum moved past m_ref + tau
     for (int j = 0; j < T; ++j) {
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
       okw = __all_sync(0xffffffffu, okw);
@@ -441,9 +442,11 @@ __global__ void __maxnreg__(C::MAXREG)
       if constexpr (C::SPLIT == 1 && !C::TF32 && C::COLS <= 64) {
         // Fast path for a full tile once every row of the warp has a reference maximum: P is
         // computed against m_ref while the scores are still arriving, 32 columns at a time (the
-        // load of the next chunk overlaps the work on this one), and the tile's extreme is
-        // tracked alongside.  If some row's maximum moved past m_ref + tau the warp falls
-        // through to the general path below, which reloads S (not yet overwritten) and rescales.
+        // load of the next chunk overlaps the work on this one).  No row maximum is formed: the
+        // row sum bounds every P of the row, so a sum of at most 2^tau shows that no score moved
+        // past m_ref + tau.  Otherwise (rarely, and always when a maximum did move) the warp falls
+        // through to the general path below, which reloads S (not yet overwritten), takes the row
+        // maxima and rescales where needed.
         // Only for 64-column tiles: with 128 columns the extra live registers spill and the
         // d = 128 kernel measured 25% slower.
         if (__all_sync(0xffffffffu, valid >= C::COLS && m_ref != -INFINITY)) {
@@ -456,19 +459,17 @@ __global__ void __maxnreg__(C::MAXREG)
           uint32_t sc[2][32];
           uint32_t pk[C::PCOLS_W / 32][32];
           uint64_t rs2[2] = {0ull, 0ull};
-          float ext = c >= 0.f ? -INFINITY : INFINITY;
           tmem_ld32(tS, sc[0]);
           tmem_wait_ld();
           reg_fence(sc[0]);
 #pragma unroll
           for (int cc = 0; cc < C::COLS / 32; ++cc) {
             if (cc + 1 < C::COLS / 32) tmem_ld32(tS + (cc + 1) * 32, sc[(cc + 1) & 1]);
-            const uint32_t(&cur)[1][32] = reinterpret_cast<const uint32_t(&)[1][32]>(sc[cc & 1]);
-            ext = c >= 0.f ? fmaxf(ext, row_extreme<32, true>(cur)) : fminf(ext, row_extreme<32, false>(cur));
+            const uint32_t(&cur)[32] = sc[cc & 1];
 #pragma unroll
             for (int qc = 0; qc < 16; ++qc) {
-              const uint64_t x = f2_fma(f2_pack(__uint_as_float(cur[0][2 * qc]), __uint_as_float(cur[0][2 * qc + 1])),
-                                        c2, negm2);
+              const uint64_t x = f2_fma(f2_pack(__uint_as_float(cur[2 * qc]), __uint_as_float(cur[2 * qc + 1])), c2,
+                                        negm2);
               float x0, x1;
               f2_unpack_f(x, x0, x1);
               const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -481,18 +482,18 @@ __global__ void __maxnreg__(C::MAXREG)
               reg_fence(sc[(cc + 1) & 1]);
             }
           }
-          const float m_tile = ext * c;
-          if (!__any_sync(0xffffffffu, m_tile > m_ref + p.tau)) {
+          float r0, r1, r2, r3;
+          f2_unpack_f(rs2[0], r0, r1);
+          f2_unpack_f(rs2[1], r2, r3);
+          const float l_tile = (r0 + r1) + (r2 + r3);
+          if (__all_sync(0xffffffffu, l_tile <= p_lim)) {
 #pragma unroll
             for (int i = 0; i < C::PCOLS_W / 32; ++i) tmem_st32(tP + i * 32, pk[i]);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_pf(t));
-            float r0, r1, r2, r3;
-            f2_unpack_f(rs2[0], r0, r1);
-            f2_unpack_f(rs2[1], r2, r3);
-            l += (r0 + r1) + (r2 + r3);
+            l += l_tile;
             continue;
           }
         }
