@@ -206,12 +206,21 @@ __global__ void __maxnreg__(C::MAXREG)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // blockIdx.x = (split * BH + bh) * n_qblk + qb: CTAs sharing a head and key range are adjacent.
-  // With a causal mask the query blocks run last-to-first, so the longest CTAs start first.
-  const int qb = p.causal ? p.n_qblk - 1 - static_cast<int>(blockIdx.x % p.n_qblk)
-                          : static_cast<int>(blockIdx.x % p.n_qblk);
-  const int bh = (blockIdx.x / p.n_qblk) % p.BH;
-  const int split = blockIdx.x / (p.n_qblk * p.BH);
+  // Without a mask, blockIdx.x = (split * BH + bh) * n_qblk + qb: CTAs sharing a head and key range
+  // are adjacent.  With a causal mask a CTA's work grows with its query block, so the query block is
+  // the slowest index, last block first: blockIdx.x = (n_qblk - 1 - qb) * (n_split * BH) + split * BH
+  // + bh.  The longest CTAs start first and the shortest fill the last wave.
+  int qb, bh, split;
+  if (p.causal) {
+    const int per_qb = p.n_split * p.BH;
+    qb = p.n_qblk - 1 - static_cast<int>(blockIdx.x / per_qb);
+    bh = static_cast<int>(blockIdx.x % per_qb) % p.BH;
+    split = static_cast<int>(blockIdx.x % per_qb) / p.BH;
+  } else {
+    qb = static_cast<int>(blockIdx.x % p.n_qblk);
+    bh = static_cast<int>(blockIdx.x / p.n_qblk) % p.BH;
+    split = static_cast<int>(blockIdx.x / (p.n_qblk * p.BH));
+  }
   const int kvh = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);  // key/value head of this query head
   const int q0 = qb * C::BR * C::NQT;
   const int k_begin = split * p.kv_per_split;
@@ -219,6 +228,12 @@ __global__ void __maxnreg__(C::MAXREG)
   // keys past the causal limit of the CTA's last row are never loaded or multiplied
   const int k_hi = p.causal ? min(k_end, q0 + C::NQT * C::BR + p.causal_off) : k_end;
   const int T = k_hi > k_begin ? (k_hi - k_begin + C::BC - 1) / C::BC : 0;  // 0 only in split mode
+  // Key tiles query tile t needs: with a causal mask the tiles past its own last row's limit are
+  // skipped (no products, no softmax); the last tile needs all T.
+  auto tile_steps = [&](int t) {
+    const int hi = p.causal ? min(k_end, q0 + (t + 1) * C::BR + p.causal_off) : k_end;
+    return hi > k_begin ? (hi - k_begin + C::BC - 1) / C::BC : 0;
+  };
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_q = bar0;
@@ -369,8 +384,10 @@ __global__ void __maxnreg__(C::MAXREG)
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < C::NQT; ++t) {
-          issue_qk(t, 0);
-          commit(bar_sf(t));
+          if (tile_steps(t) > 0) {
+            issue_qk(t, 0);
+            commit(bar_sf(t));
+          }
         }
         commit(bar_ke(0));
       }
@@ -385,27 +402,33 @@ __global__ void __maxnreg__(C::MAXREG)
         if (!ok) break;
 #pragma unroll
         for (int t = 0; t < C::NQT; ++t) {
-          if constexpr (C::PV2) {  // first half of P V as soon as the first half of P is in
-            ok = wait_all(bar_ph(t), j & 1, W_PF);
+          // tile t takes part in steps j < T_t only (T_t = T for the last tile)
+          const int Tt = t == C::NQT - 1 ? T : tile_steps(t);
+          if (j < Tt) {
+            if constexpr (C::PV2) {  // first half of P V as soon as the first half of P is in
+              ok = wait_all(bar_ph(t), j & 1, W_PF);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, s, j > 0, 0, C::BC / C::MMA_K / 2);
+            }
+            ok = wait_all(bar_pf(t), j & 1, W_PF);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, s, j > 0, 0, C::BC / C::MMA_K / 2);
+            if constexpr (C::PV2)
+              issue_pv(t, s, true, C::BC / C::MMA_K / 2, C::BC / C::MMA_K);
+            else
+              issue_pv(t, s, j > 0);
           }
-          ok = wait_all(bar_pf(t), j & 1, W_PF);
-          if (!ok) break;
-          tc_fence_after();
-          if constexpr (C::PV2)
-            issue_pv(t, s, true, C::BC / C::MMA_K / 2, C::BC / C::MMA_K);
-          else
-            issue_pv(t, s, j > 0);
           if (t == C::NQT - 1) commit(bar_ve(s));
-          if (j1 < T) {
-            issue_qk(t, s1);
-            commit(bar_sf(t));
-            if (t == C::NQT - 1) commit(bar_ke(s1));
-          } else {
-            commit(bar_od(t));
+          if (j < Tt) {
+            if (j1 < Tt) {
+              issue_qk(t, s1);
+              commit(bar_sf(t));
+            } else {
+              commit(bar_od(t));
+            }
           }
+          if (t == C::NQT - 1 && j1 < T) commit(bar_ke(s1));
         }
       }
       // Drain: all MMAs issued above complete before tensor memory is freed.
@@ -435,7 +458,8 @@ __global__ void __maxnreg__(C::MAXREG)
     bool ok = true;
     const uint64_t c2 = f2_pack(c, c);
     const float p_lim = exp2f(p.tau);  // largest row sum of P that proves no maximum moved past m_ref + tau
-    for (int j = 0; j < T; ++j) {
+    const int Tt = tile_steps(t);      // key tiles of this query tile
+    for (int j = 0; j < Tt; ++j) {
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
       okw = __all_sync(0xffffffffu, okw);
       const int valid = row_lim - k_begin - j * C::BC - h * C::COLS;  // valid key columns here (may be <= 0)
@@ -625,21 +649,21 @@ __global__ void __maxnreg__(C::MAXREG)
       l = l * alpha + ((r0 + r1) + (r2 + r3));
     }
     // ---------------------------------------------------------- epilogue: O / l, LSE
-    if (ok && T > 0) {  // `ok` agrees across the warpgroups of the tile here
+    if (ok && Tt > 0) {  // `ok` agrees across the warpgroups of the tile here
       bool okw = mbar_wait(bar_od(t), 0, abort_flag, p.err, W_OD);
       okw = __all_sync(0xffffffffu, okw);
-      if constexpr (C::SPLIT > 1) {  // total row sum from the partial sums (slot T & 1 is free)
-        xch[xidx(T & 1, h)] = l;
+      if constexpr (C::SPLIT > 1) {  // total row sum from the partial sums (slot Tt & 1 is free)
+        xch[xidx(Tt & 1, h)] = l;
         ok = bar_red_and(1 + t, 128 * C::SPLIT, okw);
         float lt = 0.f;
 #pragma unroll
-        for (int hh = 0; hh < C::SPLIT; ++hh) lt += xch[xidx(T & 1, hh)];
+        for (int hh = 0; hh < C::SPLIT; ++hh) lt += xch[xidx(Tt & 1, hh)];
         l = lt;
       } else {
         ok = okw;
       }
     }
-    if (T == 0) {  // split mode, key range entirely above the causal diagonal: empty state (-inf, 0, 0)
+    if (Tt == 0) {  // split mode, key range entirely above the tile's causal diagonal: empty state (-inf, 0, 0)
       const int qrow = q0 + t * C::BR + row;
       if (qrow < p.Nq) {
         const size_t srow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + qrow;
