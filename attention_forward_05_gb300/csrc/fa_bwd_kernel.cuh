@@ -223,8 +223,12 @@ __global__ void __maxnreg__(C::MAXREG)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int kb = static_cast<int>(blockIdx.x % p.n_kblk);  // low key tiles first: with a causal mask they see most rows
-  const int kvbh = static_cast<int>(blockIdx.x / p.n_kblk);
+  // With a causal mask a key tile sees fewer query rows the later it lies, so the key tile is the
+  // slowest grid index, low tiles first: the longest CTAs of every head start in the first wave.
+  // Without a mask the key tiles of one head are adjacent.
+  const int n_kvbh = static_cast<int>(gridDim.x) / p.n_kblk;
+  const int kb = p.causal ? static_cast<int>(blockIdx.x) / n_kvbh : static_cast<int>(blockIdx.x % p.n_kblk);
+  const int kvbh = p.causal ? static_cast<int>(blockIdx.x) % n_kvbh : static_cast<int>(blockIdx.x / p.n_kblk);
   const int b = kvbh / p.Hkv;
   const int g = kvbh % p.Hkv;
   const int G = p.H / p.Hkv;  // query heads per key/value head
@@ -610,10 +614,11 @@ __global__ void __maxnreg__(C::MAXREG)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // with a causal mask the query blocks run last-to-first, so the longest CTAs start first
-  const int qb = p.causal ? p.n_qblk - 1 - static_cast<int>(blockIdx.x % p.n_qblk)
-                          : static_cast<int>(blockIdx.x % p.n_qblk);
-  const int bh = static_cast<int>(blockIdx.x / p.n_qblk);
+  // With a causal mask the query block is the slowest grid index, last block first, so the longest
+  // CTAs of every head start in the first wave; without a mask the blocks of one head are adjacent.
+  const int n_bh = static_cast<int>(gridDim.x) / p.n_qblk;
+  const int qb = p.causal ? p.n_qblk - 1 - static_cast<int>(blockIdx.x) / n_bh : static_cast<int>(blockIdx.x % p.n_qblk);
+  const int bh = p.causal ? static_cast<int>(blockIdx.x) % n_bh : static_cast<int>(blockIdx.x / p.n_qblk);
   const int kvh = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);
   const int q0 = qb * C::BR * C::NQT;
   const int k_hi = p.causal ? min(p.Nk, q0 + C::NQT * C::BR + p.causal_off) : p.Nk;
