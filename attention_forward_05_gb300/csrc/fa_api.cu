@@ -323,6 +323,32 @@ int host_pipe(int dev, HostPipe** out) {
   return FA_OK;
 }
 
+// Chunks of fa_fwd_host, in key/value-head units.  The host link (about 200 GB/s each way) moves
+// the inputs slower than the forward consumes them, so what shows besides the copies is the first
+// chunk's copy in and the last chunk's compute and copy out.  A chunk launches `unit_ctas` CTAs per
+// unit; `wave` units fill the SMs' CTA slots once.  The last chunk is kHostLastWaves waves, the others
+// about kHostRestWaves each: small enough to start early and end soon, large enough that the forward
+// keeps up with the copies.  One wave each measured best (16 MB chunks, which left the d = 128
+// forward at under a wave per launch: 696 -> 757 TFLOP/s end to end; two waves: 752; three: 711).
+// Writes bounds[0 .. n] and returns n.
+constexpr int kHostRestWaves = 1, kHostLastWaves = 1;
+int host_chunks(long long units, long long unit_ctas, long long slots, long long* bounds) {
+  const long long wave = slots / unit_ctas > 1 ? slots / unit_ctas : 1;
+  const long long last = units < kHostLastWaves * wave ? units : kHostLastWaves * wave;
+  const long long rest = units - last;
+  long long n_rest = 0;
+  if (rest > 0) {
+    const long long per = kHostRestWaves * wave;
+    n_rest = (rest + per / 2) / per;
+    if (n_rest < 1) n_rest = 1;
+    if (n_rest > kHostMaxChunks - 1) n_rest = kHostMaxChunks - 1;
+  }
+  bounds[0] = 0;
+  for (long long i = 1; i <= n_rest; ++i) bounds[i] = rest * i / n_rest;
+  bounds[n_rest + 1] = units;
+  return static_cast<int>(n_rest + 1);
+}
+
 // Device layout of fa_fwd_host's workspace: q, k, v, o, lse, each 256-byte aligned.
 struct HostLayout {
   size_t q = 0, k = 0, v = 0, o = 0, lse = 0, total = 0;
@@ -361,9 +387,9 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   if (rc != FA_OK) return rc;
   const HostLayout lay = host_layout(B, H, Hkv, Nq, Nk, d, dtype);
   if (workspace && workspace_bytes < lay.total) return FA_ERR_INVALID_ARG;
-  int dev = 0;
+  int dev = 0, sms = 0;
   int* err = nullptr;
-  if ((rc = device_setup(&dev, &err)) != FA_OK) return rc;
+  if ((rc = device_setup(&dev, &err, &sms)) != FA_OK) return rc;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
@@ -382,22 +408,20 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     return rc;
   }
   // Chunks of whole key/value heads (each with its H / Hkv query heads): q, k, v, o and lse of a chunk
-  // are contiguous ranges.  About 16 MB of input per chunk, at most kHostMaxChunks: the first chunk's
-  // copy in and the last chunk's copy out are the parts that nothing overlaps.
+  // are contiguous ranges.
   const size_t esz = dtype == FA_BF16 ? 2 : 4;
   const int G = H / Hkv;
   const long long units = static_cast<long long>(B) * Hkv;
   const size_t q_unit = static_cast<size_t>(G) * Nq * d * esz, kv_unit = static_cast<size_t>(Nk) * d * esz;
-  const size_t in_bytes = static_cast<size_t>(units) * (q_unit + 2 * kv_unit);
-  long long n = static_cast<long long>((in_bytes + (16u << 20) - 1) / (16u << 20));
-  if (n > kHostMaxChunks) n = kHostMaxChunks;
-  if (n > units) n = units;
-  if (n < 1) n = 1;
+  const fa::FwdGeometry geo = fa::fwd_geometry(dtype == FA_BF16 ? 1 : 0, d);
+  const long long unit_ctas = static_cast<long long>(G) * ((Nq + geo.rows_per_cta - 1) / geo.rows_per_cta);
+  long long bounds[kHostMaxChunks + 1];
+  const int n = host_chunks(units, unit_ctas, static_cast<long long>(sms) * geo.ctas_per_sm, bounds);
   cudaError_t e = cudaEventRecord(hp->ev_start, st);  // device buffers may still be in use by earlier work
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->s_in, hp->ev_start, 0);
   int status = FA_OK;
-  for (long long c = 0; c < n && e == cudaSuccess && status == FA_OK; ++c) {
-    const long long u0 = units * c / n, u1 = units * (c + 1) / n;
+  for (int c = 0; c < n && e == cudaSuccess && status == FA_OK; ++c) {
+    const long long u0 = bounds[c], u1 = bounds[c + 1];
     const size_t nu = static_cast<size_t>(u1 - u0);
     char* dq = ws + lay.q + u0 * q_unit;
     char* dk = ws + lay.k + u0 * kv_unit;

@@ -506,10 +506,15 @@ def measure_e2e(fa, torch, pre, dec, stream, steps, flops_step, dec_bytes):
     wstreams = {n: torch.cuda.Stream(device=stream.device) for n in pre}
     ev_go, ev_done = torch.cuda.Event(), {n: torch.cuda.Event() for n in pre}
 
+    # The larger problem is enqueued first: its copies go first on the shared host link, and the
+    # smaller one's last chunk is then the only compute and copy-out left after the last copy in.
+    pre_order = sorted(pre, key=lambda n: -pre[n][1].numel())
+
     def pre_step():
         # the library's host-buffer entry point: copies in and out overlap the compute, chunk by chunk
         ev_go.record(stream)
-        for n, (w, q, k, v, o, lse) in pre.items():
+        for n in pre_order:
+            w, q, k, v, o, lse = pre[n]
             hq, hk, hv, ho, hl, ws = host[n]
             wstreams[n].wait_event(ev_go)
             fa.fa_fwd_host(hq, hk, hv, scale=w.scale, o=ho, lse=hl, workspace=ws, stream=wstreams[n])

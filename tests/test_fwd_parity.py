@@ -193,3 +193,20 @@ def test_fwd_host_buffers(cuda_device, dtype, causal, hkv):
     assert (lse - ld.cpu()).abs().max().item() <= 1e-3
     rows = sample_rows(N, 24, 3102)
     check_fwd(q, k, v, o, lse, 1 / math.sqrt(d), rows=rows, name=f"fwd_host {dtype} causal={causal}", causal=causal)
+
+
+def test_fwd_host_many_chunks(cuda_device):
+    """Enough key/value heads that fa_fwd_host copies and computes in several chunks (one wave of
+    CTAs each): every head's output matches the single device launch."""
+    B, H, N, d = 8, 64, 256, 128
+    q, k, v = make_qkv(B, H, N, N, d, "bf16", seed=3110)
+    hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+    o, lse = fa.fa_fwd_host(hq, hk, hv)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    od, ld = fa.fa_fwd(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device))
+    torch.cuda.synchronize()
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+    rows = sample_rows(N, 8, 3111)
+    check_fwd(q[:1], k[:1], v[:1], o[:1], lse[:1], 1 / math.sqrt(d), rows=rows, name="fwd_host chunks first batch")
+    check_fwd(q[-1:], k[-1:], v[-1:], o[-1:], lse[-1:], 1 / math.sqrt(d), rows=rows, name="fwd_host chunks last batch")
