@@ -109,9 +109,10 @@ size_t fa_fwd_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int 
 /*
  * fa_fwd_host -- fa_fwd_ex (kv_splits = 0) on HOST-resident tensors: the library
  * copies q, k, v to the device, computes, and copies o and lse back, in chunks
- * of whole key/value heads so that the copies of one chunk overlap the compute of
- * the previous one (copy-in and copy-out on two internal streams, compute on
- * `stream`, ordered by events).  The exact attention computed is fa_fwd_ex's.
+ * of whole key/value heads (as many as fill the GPU's CTA slots once) so that the
+ * copies of one chunk overlap the compute of the previous one (copy-in and
+ * copy-out on two internal streams, compute on `stream`, ordered by events).  The
+ * exact attention computed is fa_fwd_ex's.
  *   q, k, v, o, lse   HOST pointers, same shapes and dtypes as fa_fwd_ex; lse may
  *                     be NULL.  Page-locked (pinned) memory is needed for the
  *                     copies to overlap; pageable memory works but serialises.
