@@ -3,6 +3,8 @@
 //
 // Source: "Flash Attention 代码填空 (Level 2-3)", Exercise 5 (recompute P from the saved row
 // statistics, dV_j += P_ij^T dO_i); the remaining gradients are the chain rule through the softmax.
+#include <utility>
+
 #include "fa_bwd_kernel.cuh"
 
 namespace fa {
@@ -41,6 +43,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
                                                           const uint16_t* __restrict__ dout,
                                                           const float* __restrict__ lse, float* __restrict__ rowv,
                                                           long long rows_pad, int Nq, int Nq_pad) {
+  griddep_launch_dependents();  // the dK/dV kernel may start its set-up; it waits for this grid's rows
   constexpr int LPR = D / 8;  // lanes per row
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long r = gt / LPR;
@@ -84,6 +87,24 @@ cudaError_t launch_bwd_prep(const BwdLaunch& a) {
   return cudaGetLastError();
 }
 
+// Launch with programmatic stream serialization: the kernel may start before the previous kernel in
+// the stream has completed, once every CTA of that kernel has executed griddepcontrol.launch_dependents.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, int threads, int smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <class C>
 cudaError_t launch_dkdv(const BwdLaunch& a) {
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -109,9 +130,8 @@ cudaError_t launch_dkdv(const BwdLaunch& a) {
   if (p.n_qt * C::BQ > a.Nq_pad) return cudaErrorInvalidValue;  // the vectors are read in whole steps
   const long long grid = static_cast<long long>(p.n_kblk) * a.BHkv;
   if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  fa_bwd_dkdv_kernel<C><<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream>>>(
-      *a.tm_k_kv, *a.tm_v_kv, *a.tm_q_kv, *a.tm_do_kv, p);
-  return cudaGetLastError();
+  return launch_dependent(fa_bwd_dkdv_kernel<C>, static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream,
+                          *a.tm_k_kv, *a.tm_v_kv, *a.tm_q_kv, *a.tm_do_kv, p);
 }
 
 template <class C>
@@ -135,9 +155,11 @@ cudaError_t launch_dq(const BwdLaunch& a) {
   p.scale = a.scale;
   const long long grid = static_cast<long long>(p.n_qblk) * a.BH;
   if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  fa_bwd_dq_kernel<C><<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream>>>(
-      *a.tm_q_q, *a.tm_do_q, *a.tm_k_q, *a.tm_v_q, p);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the dK/dV kernel, which it does not read (the row values
+  // of the prep kernel are complete once every dK/dV CTA has passed its wait): its CTAs fill the
+  // SMs that the dK/dV grid's last wave leaves idle.
+  return launch_dependent(fa_bwd_dq_kernel<C>, static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream,
+                          *a.tm_q_q, *a.tm_do_q, *a.tm_k_q, *a.tm_v_q, p);
 }
 
 BwdGeometry bwd_geometry(int d) {

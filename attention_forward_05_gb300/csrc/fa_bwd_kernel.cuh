@@ -283,6 +283,11 @@ __global__ void __maxnreg__(C::MAXREG)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent of the prep kernel: the set-up above overlaps its tail, and
+  // the row values it writes are read only after this wait.  Then the dQ kernel launched after this
+  // one (it reads nothing this kernel writes) may take the SMs this grid's last wave leaves idle.
+  griddep_wait();
+  griddep_launch_dependents();
 
   auto step_head = [&](int s) { return b * p.H + g * G + s / per_head; };  // query (batch, head) index
   auto step_qt = [&](int s) { return i_lo + s % per_head; };               // query tile
@@ -878,6 +883,9 @@ __global__ void __maxnreg__(C::MAXREG)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+  // When this grid overlaps the tail of the dK/dV grid (programmatic launch), it completes only after
+  // that grid has: work enqueued after the backward sees all three gradients.
+  griddep_wait();
 }
 
 }  // namespace fa

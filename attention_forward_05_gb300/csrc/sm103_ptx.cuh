@@ -255,6 +255,13 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt, int M, int N, in
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
+// Programmatic dependent launch: a kernel launched after this one with the programmatic stream
+// serialization attribute may start once every CTA of this grid has executed launch_dependents (or
+// exited); griddep_wait blocks until the grid this one depends on has completed and its memory
+// operations are visible (a no-op for a kernel launched without the attribute).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- math
 
 __device__ __forceinline__ float ex2_approx(float x) {
