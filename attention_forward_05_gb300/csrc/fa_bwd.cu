@@ -3,8 +3,6 @@
 //
 // Source: "Flash Attention 代码填空 (Level 2-3)", Exercise 5 (recompute P from the saved row
 // statistics, dV_j += P_ij^T dO_i); the remaining gradients are the chain rule through the softmax.
-#include <utility>
-
 #include "fa_bwd_kernel.cuh"
 
 namespace fa {
@@ -85,24 +83,6 @@ cudaError_t launch_bwd_prep(const BwdLaunch& a) {
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.lse, a.rowv, rows, a.Nq,
         a.Nq_pad);
   return cudaGetLastError();
-}
-
-// Launch with programmatic stream serialization: the kernel may start before the previous kernel in
-// the stream has completed, once every CTA of that kernel has executed griddepcontrol.launch_dependents.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, int threads, int smem, cudaStream_t stream,
-                             Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(static_cast<unsigned>(threads));
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <class C>

@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(DEC_THREADS) fa_decode_split_kernel(
   constexpr int KPW = 32 / LPK;  // key rows per warp-wide load
   constexpr int U = DEC_UNROLL;
   __shared__ float sm_m[DEC_WARPS], sm_l[DEC_WARPS];
+  griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to complete
   __shared__ float sm_o[DEC_WARPS][D];
 
   const int split = blockIdx.x % splits;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_decode_merge_kernel(
   constexpr int PER = D / 32;  // output dimensions per lane (lane-strided)
   __shared__ unsigned seen[MAX_SPLITS / 32];
   __shared__ int bad;
+  griddep_wait();  // launched as a programmatic dependent of the split kernel that writes the states
   if (order != nullptr) {  // the order must be a permutation of 0..splits-1
     for (int i = threadIdx.x; i < (splits + 31) / 32; i += blockDim.x) seen[i] = 0u;
     if (threadIdx.x == 0) bad = 0;
@@ -241,10 +243,8 @@ static cudaError_t launch_decode_d(const DecodeLaunch& a) {
   if (e != cudaSuccess) return e;
   const int heads_per_cta = MERGE_THREADS / 32;
   const unsigned grid2 = static_cast<unsigned>((a.BH + heads_per_cta - 1) / heads_per_cta);
-  fa_decode_merge_kernel<D><<<grid2, MERGE_THREADS, 0, a.stream>>>(ws_m, ws_l, ws_o, a.order,
-                                                                  static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH,
-                                                                  a.splits);
-  return cudaGetLastError();
+  return launch_dependent(fa_decode_merge_kernel<D>, grid2, MERGE_THREADS, 0, a.stream, ws_m, ws_l, ws_o, a.order,
+                          static_cast<__nv_bfloat16*>(a.o), a.lse, a.BH, a.splits);
 }
 
 cudaError_t launch_decode_merge(const float* ws_m, const float* ws_l, const float* ws_o, const int* order, void* o,
@@ -252,15 +252,14 @@ cudaError_t launch_decode_merge(const float* ws_m, const float* ws_l, const floa
   if (splits < 1 || splits > MAX_SPLITS || BH < 1) return cudaErrorInvalidValue;
   const int heads_per_cta = MERGE_THREADS / 32;
   const unsigned grid = static_cast<unsigned>((BH + heads_per_cta - 1) / heads_per_cta);
+  // a programmatic dependent of the split kernel that wrote the states
   if (d == 64)
-    fa_decode_merge_kernel<64><<<grid, MERGE_THREADS, 0, stream>>>(ws_m, ws_l, ws_o, order,
-                                                                  static_cast<__nv_bfloat16*>(o), lse, BH, splits);
-  else if (d == 128)
-    fa_decode_merge_kernel<128><<<grid, MERGE_THREADS, 0, stream>>>(ws_m, ws_l, ws_o, order,
-                                                                   static_cast<__nv_bfloat16*>(o), lse, BH, splits);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+    return launch_dependent(fa_decode_merge_kernel<64>, grid, MERGE_THREADS, 0, stream, ws_m, ws_l, ws_o, order,
+                            static_cast<__nv_bfloat16*>(o), lse, BH, splits);
+  if (d == 128)
+    return launch_dependent(fa_decode_merge_kernel<128>, grid, MERGE_THREADS, 0, stream, ws_m, ws_l, ws_o, order,
+                            static_cast<__nv_bfloat16*>(o), lse, BH, splits);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeLaunch& a) {

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) fa_decode_gqa_split_kern
     float* __restrict__ ws_m, float* __restrict__ ws_l, float* __restrict__ ws_o, int* err, int Nk, int splits,
     int L, int H, int Hkv, int qgroups, float c) {
   constexpr int D = C::D, G = C::G, GW = C::GW;
+  griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to complete
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float sm_m[C::WPS][G], sm_l[C::WPS][G];
   __shared__ float sm_o[C::WPS][G][D];

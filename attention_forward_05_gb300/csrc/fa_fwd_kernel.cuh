@@ -279,6 +279,9 @@ __global__ void __maxnreg__(C::MAXREG)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // A merge kernel launched after this one (split mode) may be scheduled once every CTA has started;
+  // it waits for this grid's completion before it reads the partial states.
+  griddep_launch_dependents();
 
   if (warp == C::LOAD_WARP) {
     // ------------------------------------------------------------ TMA producer

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_CTA)
   constexpr int PER = D / 32;
   __shared__ unsigned seen[MERGE_MAX_SPLITS / 32];
   __shared__ int bad;
+  griddep_wait();  // launched as a programmatic dependent of the kernel that writes the partial states
   if (order != nullptr) {  // the order must be a permutation of 0 .. n_split - 1
     for (int i = threadIdx.x; i < (n_split + 31) / 32; i += blockDim.x) seen[i] = 0u;
     if (threadIdx.x == 0) bad = 0;
@@ -77,13 +78,14 @@ cudaError_t launch_fwd_merge(const float* ws_o, const float* ws_ml, void* o, flo
                              int n_split, int out_bf16, cudaStream_t stream, const int* order) {
   const long long grid = (rows + MERGE_ROWS_PER_CTA - 1) / MERGE_ROWS_PER_CTA;
   if (grid <= 0 || grid > 0x7FFFFFFFLL || n_split < 1 || n_split > MERGE_MAX_SPLITS) return cudaErrorInvalidValue;
-  const dim3 g(static_cast<unsigned>(grid)), b(32 * MERGE_ROWS_PER_CTA);
+  const unsigned g = static_cast<unsigned>(grid);
+  const int b = 32 * MERGE_ROWS_PER_CTA;
   const float2* ml = reinterpret_cast<const float2*>(ws_ml);
-  if (d == 64 && out_bf16) fa_fwd_merge_kernel<64, true><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
-  else if (d == 64) fa_fwd_merge_kernel<64, false><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
-  else if (out_bf16) fa_fwd_merge_kernel<128, true><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
-  else fa_fwd_merge_kernel<128, false><<<g, b, 0, stream>>>(ws_o, ml, o, lse, rows, n_split, order);
-  return cudaGetLastError();
+  // a programmatic dependent of the forward that wrote the states: its launch overlaps that grid's tail
+  if (d == 64 && out_bf16) return launch_dependent(fa_fwd_merge_kernel<64, true>, g, b, 0, stream, ws_o, ml, o, lse, rows, n_split, order);
+  if (d == 64) return launch_dependent(fa_fwd_merge_kernel<64, false>, g, b, 0, stream, ws_o, ml, o, lse, rows, n_split, order);
+  if (out_bf16) return launch_dependent(fa_fwd_merge_kernel<128, true>, g, b, 0, stream, ws_o, ml, o, lse, rows, n_split, order);
+  return launch_dependent(fa_fwd_merge_kernel<128, false>, g, b, 0, stream, ws_o, ml, o, lse, rows, n_split, order);
 }
 
 }  // namespace fa

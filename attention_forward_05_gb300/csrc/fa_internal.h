@@ -5,7 +5,27 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace fa {
+
+// Launch with programmatic stream serialization: the kernel may start before the previous kernel in
+// the stream has completed, once every CTA of that kernel has executed griddepcontrol.launch_dependents.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, int threads, int smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct FwdLaunch {
   const CUtensorMap* tm_q;  // 3-D maps over [B*H, N, d] (innermost d), 128-byte swizzle
