@@ -274,6 +274,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.tau = 8.0f;
   a.fault = g_fault.exchange(0);
   a.stream = st;
+  a.dependent = geo.v_kmajor ? 1 : 0;  // the fp32 prep kernel was the last launch on `st`
   cudaError_t e;
   if (bf16)
     e = (d == 64) ? fa::launch_fwd_bf16_d64(a) : fa::launch_fwd_bf16_d128(a);

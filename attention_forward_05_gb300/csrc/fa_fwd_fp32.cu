@@ -27,55 +27,66 @@ __device__ __forceinline__ float round_tf32(float x) {
   return __uint_as_float(r);
 }
 
-// One 32 x 32 block per CTA, staged through shared memory so that both the
-// read of V rows and the write of V^T rows are coalesced.
-__global__ void __launch_bounds__(256) transpose_v_kernel(const float* __restrict__ v, float* __restrict__ vt,
-                                                          int Nk, int Nk_pad, int d, int n_kb) {
-  __shared__ float tile[32][33];
-  const int bh = blockIdx.x / n_kb;
-  const int j0 = (blockIdx.x % n_kb) * 32;
-  const int c0 = blockIdx.y * 32;
-  const float* vb = v + static_cast<size_t>(bh) * Nk * d;
-  float* tb = vt + static_cast<size_t>(bh) * d * Nk_pad;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int j = j0 + r;
-    tile[r][threadIdx.x] = (j < Nk) ? round_tf32(vb[static_cast<size_t>(j) * d + c0 + threadIdx.x]) : 0.f;
+// The prep pass, one launch: CTAs [0, n_tr) transpose V in 32 x 32 blocks (staged through shared
+// memory so that both the read of V rows and the write of V^T rows are coalesced; block t covers key
+// rows 32 (t % n_kb) .. and columns 32 (t / n_kb % (d / 32)) .. of head t / (n_kb d / 32)); the rest
+// copy Q and K rounded to the nearest tf32 value (n4q, n4k float4s, 16-byte aligned pointers).
+__global__ void __launch_bounds__(256) prep_fp32_kernel(const float* __restrict__ v, float* __restrict__ vt,
+                                                        const float4* __restrict__ q, float4* __restrict__ qr,
+                                                        size_t n4q, const float4* __restrict__ k,
+                                                        float4* __restrict__ kr, size_t n4k, int Nk, int Nk_pad,
+                                                        int d, int n_kb, long long n_tr) {
+  griddep_launch_dependents();  // the forward may do its set-up; it waits for this grid's outputs
+  if (static_cast<long long>(blockIdx.x) < n_tr) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int ncb = d / 32;
+    const long long t = blockIdx.x;
+    const int kb = static_cast<int>(t % n_kb);
+    const int cb = static_cast<int>((t / n_kb) % ncb);
+    const long long bh = t / (static_cast<long long>(n_kb) * ncb);
+    const int j0 = kb * 32, c0 = cb * 32;
+    const float* vb = v + static_cast<size_t>(bh) * Nk * d;
+    float* tb = vt + static_cast<size_t>(bh) * d * Nk_pad;
+    for (int r = ty; r < 32; r += 8) {
+      const int j = j0 + r;
+      tile[r][tx] = (j < Nk) ? round_tf32(vb[static_cast<size_t>(j) * d + c0 + tx]) : 0.f;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+      const int j = j0 + tx;
+      if (j < Nk_pad) tb[static_cast<size_t>(c0 + r) * Nk_pad + j] = tile[tx][r];
+    }
+    return;
   }
-  __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int j = j0 + threadIdx.x;
-    if (j < Nk_pad) tb[static_cast<size_t>(c0 + r) * Nk_pad + j] = tile[threadIdx.x][r];
-  }
-}
-
-// Element-wise round-to-nearest tf32 copy (n a multiple of 4, 16-byte aligned pointers).
-__global__ void __launch_bounds__(256) round_tf32_kernel(const float4* __restrict__ x, float4* __restrict__ y,
-                                                         size_t n4) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    float4 a = x[i];
+  const size_t n4 = n4q + n4k;
+  const size_t stride = (gridDim.x - static_cast<size_t>(n_tr)) * blockDim.x;
+  for (size_t i = (blockIdx.x - static_cast<size_t>(n_tr)) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 a = i < n4q ? q[i] : k[i - n4q];
     a.x = round_tf32(a.x);
     a.y = round_tf32(a.y);
     a.z = round_tf32(a.z);
     a.w = round_tf32(a.w);
-    y[i] = a;
+    if (i < n4q)
+      qr[i] = a;
+    else
+      kr[i - n4q] = a;
   }
 }
 
 cudaError_t launch_prep_fp32(const float* q, const float* k, const float* v, float* qr, float* kr, float* vt,
                              int BH, int BHkv, int Nq, int Nk, int Nk_pad, int d, cudaStream_t stream) {
   const int n_kb = (Nk_pad + 31) / 32;
-  const long long gx = static_cast<long long>(n_kb) * BHkv;
-  if (gx <= 0 || gx > 0x7FFFFFFFLL || d % 32 != 0) return cudaErrorInvalidValue;
-  transpose_v_kernel<<<dim3(static_cast<unsigned>(gx), d / 32), dim3(32, 8), 0, stream>>>(v, vt, Nk, Nk_pad, d,
-                                                                                         n_kb);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  const long long n_tr = static_cast<long long>(n_kb) * (d / 32) * BHkv;
+  if (n_tr <= 0 || d % 32 != 0) return cudaErrorInvalidValue;
   const size_t nq4 = static_cast<size_t>(BH) * Nq * d / 4, nk4 = static_cast<size_t>(BHkv) * Nk * d / 4;
-  const unsigned gq = static_cast<unsigned>(nq4 / 256 + 1 < 4096 ? nq4 / 256 + 1 : 4096);
-  const unsigned gk = static_cast<unsigned>(nk4 / 256 + 1 < 4096 ? nk4 / 256 + 1 : 4096);
-  round_tf32_kernel<<<gq, 256, 0, stream>>>(reinterpret_cast<const float4*>(q), reinterpret_cast<float4*>(qr), nq4);
-  round_tf32_kernel<<<gk, 256, 0, stream>>>(reinterpret_cast<const float4*>(k), reinterpret_cast<float4*>(kr), nk4);
+  const size_t n4 = nq4 + nk4;
+  const long long n_round = static_cast<long long>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
+  const long long grid = n_tr + n_round;
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  prep_fp32_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      v, vt, reinterpret_cast<const float4*>(q), reinterpret_cast<float4*>(qr), nq4,
+      reinterpret_cast<const float4*>(k), reinterpret_cast<float4*>(kr), nk4, Nk, Nk_pad, d, n_kb, n_tr);
   return cudaGetLastError();
 }
 

@@ -279,8 +279,11 @@ __global__ void __maxnreg__(C::MAXREG)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // A merge kernel launched after this one (split mode) may be scheduled once every CTA has started;
+  // After the fp32 prep kernel this grid is its programmatic dependent: the set-up above overlapped
+  // that kernel, whose rounded Q, K and V^T are read only after this wait (a no-op otherwise).  A
+  // merge kernel launched after this one (split mode) may be scheduled once every CTA has started;
   // it waits for this grid's completion before it reads the partial states.
+  griddep_wait();
   griddep_launch_dependents();
 
   if (warp == C::LOAD_WARP) {
@@ -778,6 +781,9 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
     return cudaErrorInvalidValue;  // every split must own at least one key
   const long long grid = static_cast<long long>(p.n_qblk) * a.BH * a.n_split;
   if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  if (a.dependent)
+    return launch_dependent(fa_fwd_kernel<C>, static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream,
+                            *a.tm_q, *a.tm_k, *a.tm_v, p);
   fa_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream>>>(*a.tm_q, *a.tm_k,
                                                                                         *a.tm_v, p);
   return cudaGetLastError();

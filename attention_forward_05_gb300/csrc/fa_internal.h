@@ -45,6 +45,7 @@ struct FwdLaunch {
   float tau;                // lazy-rescale threshold in log2 units (0 = rescale whenever m grows)
   int fault;                // test-only fault injection mode (0 = none)
   cudaStream_t stream;
+  int dependent = 0;        // 1: the fp32 prep kernel precedes it on `stream` (programmatic dependent launch)
 };
 
 // Tile geometry the tensor maps must be encoded with, per instantiation.
