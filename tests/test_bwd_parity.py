@@ -153,3 +153,23 @@ def test_bwd_full_size_d128_properties(cuda_device):
     print(f"[parity] bwd full d128 identities: sum dV vs sum dO {e_v:.3e}, |sum dK| {e_k:.3e}")
     # each sum has 8192 terms, each carrying a relative rounding of about u = 2^-8
     assert e_v <= 2.0 ** -8 and e_k <= 2.0 ** -8
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_stream_order(cuda_device, d):
+    """The three backward kernels overlap one another (programmatic dependent launches), but work
+    enqueued after fa_bwd on the same stream still sees all three gradients complete: copies taken
+    right after the call, with no synchronisation in between, equal the gradients read later."""
+    B, H, N = 4, 16, 2048  # several waves of the dK/dV grid, so its tail overlaps the dQ grid
+    q, k, v = make_qkv(B, H, N, N, d, "bf16", seed=1600 + d, device=cuda_device)
+    dout = make_dout(B, H, N, d, "bf16", seed=1601 + d, device=cuda_device)
+    o, lse = fa.fa_fwd(q, k, v)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        grads = fa.fa_bwd(q, k, v, o, dout, lse)
+        early = [g.clone() for g in grads]  # enqueued right behind the dQ kernel
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    for name, g, e in zip(("dq", "dk", "dv"), grads, early):
+        assert torch.equal(g, e), name

@@ -86,3 +86,16 @@ def test_decode_workload_full_size(cuda_device):
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
     heads = np.sort(np.random.default_rng(w.seed).choice(w.B * w.H, size=64, replace=False))
     check_decode(q, k, v, o, lse, w.scale, w.splits, order, heads=heads, name=w.name)
+
+
+def test_merge_stream_order(cuda_device):
+    """The merge kernel is launched as a dependent of the split kernel; work enqueued after the call
+    sees the merged output complete."""
+    q, k, v = make_qkv(8, 16, 1, 16384, 64, "bf16", seed=1700, device=cuda_device)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o, lse = fa.fa_decode_splitkv_ex(q, k, v, 16, with_lse=True)
+        early_o, early_lse = o.clone(), lse.clone()
+    torch.cuda.synchronize()
+    assert torch.equal(o, early_o) and torch.equal(lse, early_lse)

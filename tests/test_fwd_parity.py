@@ -210,3 +210,18 @@ def test_fwd_host_many_chunks(cuda_device):
     rows = sample_rows(N, 8, 3111)
     check_fwd(q[:1], k[:1], v[:1], o[:1], lse[:1], 1 / math.sqrt(d), rows=rows, name="fwd_host chunks first batch")
     check_fwd(q[-1:], k[-1:], v[-1:], o[-1:], lse[-1:], 1 / math.sqrt(d), rows=rows, name="fwd_host chunks last batch")
+
+
+def test_fp32_split_stream_order(cuda_device):
+    """fp32 with automatic key splits runs prep -> forward -> merge, the later two as dependent
+    launches; work enqueued after the call sees the finished output."""
+    w = WORKLOADS["long_fp32"]
+    q, k, v = workload_inputs(w, device=cuda_device)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o, lse = fa.fa_fwd(q, k, v, scale=w.scale)
+        early_o, early_lse = o.clone(), lse.clone()
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    assert torch.equal(o, early_o) and torch.equal(lse, early_lse)
