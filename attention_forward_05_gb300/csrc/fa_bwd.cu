@@ -26,9 +26,14 @@ namespace fa {
 #ifndef FA_BWD_Q128_HALF
 #define FA_BWD_Q128_HALF 1
 #endif
+// ATMEM (d = 64 only: tensor memory has no room at d = 128): the dQ kernel's S and dP MMAs take Q and
+// dO from tensor memory.
+#ifndef FA_BWD_Q64_ATMEM
+#define FA_BWD_Q64_ATMEM 1
+#endif
 using BwdKV64 = BwdKVCfg<64, 64, 8, 3, FA_BWD_KV64_HALF != 0>;
 using BwdKV128 = BwdKVCfg<128, 64, 4, 2, FA_BWD_KV128_HALF != 0>;
-using BwdQ64 = BwdQCfg<64, 64, 4, FA_BWD_Q64_HALF != 0>;
+using BwdQ64 = BwdQCfg<64, 64, 4, FA_BWD_Q64_HALF != 0, FA_BWD_Q64_ATMEM != 0>;
 using BwdQ128 = BwdQCfg<128, 64, 2, FA_BWD_Q128_HALF != 0>;
 
 // D_i = sum_c dO_ic O_ic (fp32 over the bf16 inputs) and nl_i = -L_i log2(e) for the rows of

@@ -501,7 +501,7 @@ __global__ void __maxnreg__(C::MAXREG)
 
 // ------------------------------------------------------------------------------------------ dQ
 
-template <int D_, int BC_, int STAGES_, bool HALF_ = true>
+template <int D_, int BC_, int STAGES_, bool HALF_ = true, bool ATMEM_ = false>
 struct BwdQCfg {
   static constexpr int D = D_;
   static constexpr int BR = 128;           // query rows per tile (TMEM lanes)
@@ -509,6 +509,10 @@ struct BwdQCfg {
   static constexpr int BC = BC_;           // keys per step
   static constexpr int STAGES = STAGES_;   // ring of (K_j, V_j)
   static constexpr bool HALF = HALF_;      // dQ MMAs start on the first half of a step's keys
+  // ATMEM: the elementwise warpgroups copy Q_t and dO_t into tensor memory once, and S and dP take
+  // them as the A operand there: each MMA then reads only K or V from shared memory (an N = 64 MMA
+  // reading both operands from shared memory is bound by its bandwidth).
+  static constexpr bool ATMEM = ATMEM_;
   static constexpr int CHUNK = 64;
   static constexpr int NCH = D / CHUNK;
   static constexpr int MMA_K = 16;
@@ -522,14 +526,16 @@ struct BwdQCfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT],
-  // g_free[NQT], drain (score issuer), drain (dQ issuer), p_half[NQT]
-  static constexpr int NBAR = 1 + 4 * STAGES + 5 * NQT + 2;
+  // g_free[NQT], drain (score issuer), drain (dQ issuer), p_half[NQT], a_in_tmem[NQT]
+  static constexpr int NBAR = 1 + 4 * STAGES + 6 * NQT + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM: tile t holds S at t*2*BC and dP at t*2*BC + BC (dS, bf16 pairs, over the first BC/2 columns
-  // of S), dQ at 2*NQT*BC + t*D.
+  // of S), dQ at 2*NQT*BC + t*D; with ATMEM, Q_t and dO_t as bf16 pairs (D/2 columns each) after them.
   static constexpr int COL_DQ = 2 * NQT * BC;
-  static constexpr int TMEM_NEED = 2 * NQT * BC + NQT * D;
+  static constexpr int COL_QA = COL_DQ + NQT * D;
+  static constexpr int COL_DOA = COL_QA + NQT * (D / 2);
+  static constexpr int TMEM_NEED = 2 * NQT * BC + NQT * D + (ATMEM ? NQT * D : 0);
   static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int NWARPS = 4 * NQT + 3;
   static constexpr int NTHREADS = NWARPS * 32;
@@ -538,6 +544,7 @@ struct BwdQCfg {
   static constexpr int GRAD_WARP = 4 * NQT + 2;  // dQ
   static constexpr int MAXREG = RegBudget<NWARPS, 1>::VALUE;
   static_assert(D % CHUNK == 0 && BC % 64 == 0 && BC <= 128, "tile");
+  static_assert(!ATMEM || NCH == 1, "A operands copied into tensor memory from one 128-byte row segment");
   static_assert(TMEM_NEED <= 512, "tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -642,6 +649,7 @@ __global__ void __maxnreg__(C::MAXREG)
   const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 4 * C::NQT);
   const uint32_t bar_drain_g = bar_drain + 8u;
   auto bar_ph = [&](int t) { return bar_drain + 16u + 8u * t; };  // first half of dS written
+  auto bar_qa = [&](int t) { return bar_drain + 16u + 8u * (C::NQT + t); };  // Q_t, dO_t in TMEM (ATMEM)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -659,6 +667,7 @@ __global__ void __maxnreg__(C::MAXREG)
       mbar_init(bar_od(t), 1);
       mbar_init(bar_gf(t), 1);
       mbar_init(bar_ph(t), 4);
+      mbar_init(bar_qa(t), 4);
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain_g, 1);
@@ -739,6 +748,10 @@ __global__ void __maxnreg__(C::MAXREG)
       const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
       bool ok = wait_all(bar_q, 0, WB_Q);
+      if constexpr (C::ATMEM) {
+#pragma unroll
+        for (int t = 0; t < C::NQT; ++t) ok = ok && wait_all(bar_qa(t), 0, WB_Q);
+      }
       for (int j = 0; ok && j < T; ++j) {
         const int s = j % C::STAGES;
         ok = wait_all(bar_kf(s), (j / C::STAGES) & 1, WB_KF) && wait_all(bar_vf(s), (j / C::STAGES) & 1, WB_VF);
@@ -755,14 +768,22 @@ __global__ void __maxnreg__(C::MAXREG)
               const int e = kk * C::MMA_K;
               const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
               const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-              mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
+              if constexpr (C::ATMEM)
+                mma_ts<0>(tmem + col, tmem + C::COL_QA + t * (C::D / 2) + kk * (C::MMA_K / 2), dk0 + so + ob,
+                          idesc_s, kk > 0);
+              else
+                mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
             }
 #pragma unroll
             for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
               const int e = kk * C::MMA_K;
               const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
               const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-              mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
+              if constexpr (C::ATMEM)
+                mma_ts<0>(tmem + col + C::BC, tmem + C::COL_DOA + t * (C::D / 2) + kk * (C::MMA_K / 2),
+                          dv0 + so + ob, idesc_s, kk > 0);
+              else
+                mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
             }
           }
           __syncwarp();
@@ -832,7 +853,33 @@ __global__ void __maxnreg__(C::MAXREG)
     const uint64_t nl_2 = f2_pack(nl, nl);
     const uint64_t nd_2 = f2_pack(ndd, ndd);
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
+    if constexpr (C::ATMEM) {
+      // This thread's row of Q_t and of dO_t from shared memory (128-byte swizzle: 16-byte granule g of
+      // row r sits at granule g ^ (r % 8)) into its TMEM lane: 32-bit column c holds elements 2c, 2c + 1.
+      bool okq = mbar_wait(bar_q, 0, abort_flag, p.err, WB_Q);
+      ok = __all_sync(0xffffffffu, okq);
+      if (ok) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint8_t* src = smem + (m == 0 ? C::OFF_Q : C::OFF_DO) + t * C::Q_BYTES + row * 128;
+          uint32_t w[32];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + ((g ^ (row & 7)) << 4));
+            w[4 * g] = x.x;
+            w[4 * g + 1] = x.y;
+            w[4 * g + 2] = x.z;
+            w[4 * g + 3] = x.w;
+          }
+          tmem_st32(tmem + lane_base + (m == 0 ? C::COL_QA : C::COL_DOA) + t * (C::D / 2), w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_qa(t));
+      }
+    }
+    for (int j = 0; ok && j < T; ++j) {
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, WB_SF);
       ok = __all_sync(0xffffffffu, okw);
       if (!ok) break;
