@@ -93,6 +93,13 @@ int encode_map(CUtensorMap* map, const void* base, bool bf16, int BH, int rows, 
 
 constexpr long long kMaxElems = 1LL << 40;
 
+// Lazy rescale threshold of the forward kernels (log2 units): a row's reference maximum moves only
+// when a score exceeds it by more than this, so P <= 2^32.  P is bf16 (tf32 on the fp32 path) and the
+// accumulators fp32, all with fp32's exponent range: 2^32 costs no precision, and O stays finite for
+// any |v| below 2^(127 - 32 - log2 Nk).  A larger threshold rescales O less often: with the peaked
+// d = 128 inputs 8 corrected O in a third of the warp-steps, and 32 measured 5% faster.
+constexpr float kLazyTau = 32.0f;
+
 }  // namespace
 
 extern "C" {
@@ -271,7 +278,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.ws_ml = pl.n_split > 1 ? reinterpret_cast<float*>(ws + pl.off_wml) : nullptr;
   a.causal = causal;
   a.c = scale * 1.4426950408889634f;
-  a.tau = 8.0f;
+  a.tau = kLazyTau;
   a.fault = g_fault.exchange(0);
   a.stream = st;
   a.dependent = geo.v_kmajor ? 1 : 0;  // the fp32 prep kernel was the last launch on `st`
@@ -668,7 +675,7 @@ cudaError_t gqa_decode_forward(const void* q, const void* k, const void* v, void
                        : nullptr;
   a.causal = 0;
   a.c = scale * 1.4426950408889634f;
-  a.tau = 8.0f;
+  a.tau = kLazyTau;
   a.fault = 0;
   a.stream = st;
   cudaError_t e = (d == 64) ? fa::launch_fwd_decode_d64(a) : fa::launch_fwd_decode_d128(a);
