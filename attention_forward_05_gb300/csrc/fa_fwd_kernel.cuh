@@ -528,6 +528,62 @@ __global__ void __maxnreg__(C::MAXREG)
           }
         }
       }
+      if constexpr (C::PV2) {
+        // Fast path of the two-half hand-over, for a full tile once every row of the warp has a
+        // reference maximum: the first half's exponentials start as soon as S is loaded, with no row
+        // maximum in front of them.  The first half is handed over when its row sum is at most 2^tau
+        // (so none of its scores moved past m_ref + tau) and the second half's maximum is at most
+        // m_ref + tau: O then needs no correction.  Otherwise nothing has been stored yet and the
+        // warp falls through to the general path, which reloads S.  (Worth it only with a large tau:
+        // at tau = 8 the peaked inputs sent a third of the warp-steps down both paths.)
+        if (__all_sync(0xffffffffu, valid >= C::COLS && m_ref != -INFINITY)) {
+          if (!okw) {
+            ok = false;
+            break;
+          }
+          constexpr int HC = C::COLS / 2;
+          tc_fence_after();
+          uint32_t sv[C::COLS / 32][32];
+#pragma unroll
+          for (int i = 0; i < C::COLS / 32; ++i) tmem_ld32(tS + i * 32, sv[i]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < C::COLS / 32; ++i) reg_fence(sv[i]);
+          auto& sv_a = reinterpret_cast<uint32_t(&)[HC / 32][32]>(sv[0]);
+          auto& sv_b = reinterpret_cast<uint32_t(&)[HC / 32][32]>(sv[HC / 32]);
+          const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+          uint32_t pk[C::PCOLS_W / 32][32];
+          auto& pk_a = reinterpret_cast<uint32_t(&)[HC / 64][32]>(pk[0]);
+          auto& pk_b = reinterpret_cast<uint32_t(&)[HC / 64][32]>(pk[HC / 64]);
+          uint64_t rs_a[2] = {0ull, 0ull};
+          softmax_p_bf16<HC, false>(sv_a, pk_a, c2, negm2, HC, rs_a);
+          const float m_b = (c >= 0.f ? row_extreme<HC, true>(sv_b) : row_extreme<HC, false>(sv_b)) * c;
+          float r0, r1, r2, r3;
+          f2_unpack_f(rs_a[0], r0, r1);
+          f2_unpack_f(rs_a[1], r2, r3);
+          const float l_a = (r0 + r1) + (r2 + r3);
+          if (__all_sync(0xffffffffu, l_a <= p_lim && m_b <= m_ref + p.tau)) {
+#pragma unroll
+            for (int i = 0; i < HC / 64; ++i) tmem_st32(tP + i * 32, pk_a[i]);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ph(t));
+            uint64_t rs_b[2] = {0ull, 0ull};
+            softmax_p_bf16<HC, false>(sv_b, pk_b, c2, negm2, HC, rs_b);
+#pragma unroll
+            for (int i = 0; i < HC / 64; ++i) tmem_st32(tP + (HC / 64 + i) * 32, pk_b[i]);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_pf(t));
+            f2_unpack_f(rs_b[0], r0, r1);
+            f2_unpack_f(rs_b[1], r2, r3);
+            l += l_a + ((r0 + r1) + (r2 + r3));
+            continue;
+          }
+        }
+      }
       uint32_t sr[C::COLS / 32][32];
       float m_part = -INFINITY;
       {  // loaded even when the wait gave up (then the values are stale and unused): a conditional
