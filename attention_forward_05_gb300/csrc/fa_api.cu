@@ -207,6 +207,7 @@ size_t fa_fwd_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int 
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
               int Nk, int d, float scale, int dtype, int causal, int kv_splits, void* workspace,
               size_t workspace_bytes, fa_stream_t stream) {
+  const fa::NvtxRange nvtx_range("fa_fwd_ex");
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
@@ -387,6 +388,7 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d,
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Nq,
                 int Nk, int d, float scale, int dtype, int causal, void* workspace, size_t workspace_bytes,
                 fa_stream_t stream) {
+  const fa::NvtxRange nvtx_range("fa_fwd_host");
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (workspace && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -484,6 +486,7 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse, void* dq,
            void* dk, void* dv, int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int dtype, int causal,
            void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  const fa::NvtxRange nvtx_range("fa_bwd");
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv))
@@ -580,6 +583,7 @@ size_t fa_decode_workspace_bytes(int B, int H, int d, int splits) {
 int fa_decode_splitkv_ex(const void* q, const void* k, const void* v, void* o, int B, int H, int Nk, int d,
                          int splits, float scale, void* workspace, size_t workspace_bytes, const int* merge_order,
                          float* lse, fa_stream_t stream) {
+  const fa::NvtxRange nvtx_range("fa_decode_splitkv_ex");
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
@@ -691,6 +695,7 @@ extern "C" {
 int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv, int Nk, int d,
                           int splits, float scale, void* workspace, size_t workspace_bytes, const int* merge_order,
                           float* lse, fa_stream_t stream) {
+  const fa::NvtxRange nvtx_range("fa_decode_splitkv_gqa");
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;

@@ -63,6 +63,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, int B, int H, int Nk,
                                          int d, int splits, fa_stream_t stream) {
+  const fa::NvtxRange nvtx_range("fa_decode_splitkv_noalloc");
   if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Nk < 1 || Nk >= (1 << 30)) return FA_ERR_INVALID_ARG;

@@ -7,7 +7,18 @@
 
 #include <utility>
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace fa {
+
+// NVTX range over one C ABI call, named after the entry point, for timeline tools (Nsight Systems and
+// the like).  Header-only NVTX: without an attached tool a push or pop is a cheap no-op.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Launch with programmatic stream serialization: the kernel may start before the previous kernel in
 // the stream has completed, once every CTA of that kernel has executed griddepcontrol.launch_dependents.
