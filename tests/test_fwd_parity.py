@@ -159,6 +159,18 @@ def test_grouped_query_heads(cuda_device, dtype, H, Hkv, d):
     check_fwd(q, k, v, o, lse, sc, name=f"{dtype} gqa H={H} Hkv={Hkv} d{d}")
 
 
+@pytest.mark.parametrize("name", ["mh_prefill", "peaked_d128"])
+def test_full_size_repeatable(cuda_device, name):
+    """Five launches of a full-size workload give bit-identical O and LSE: a stand-in race check (the
+    kernels use no atomics, so any difference would come from a read racing a write)."""
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w, device=cuda_device)
+    o0, l0 = _run(q, k, v, w.scale)
+    for _ in range(4):
+        o, lse = _run(q, k, v, w.scale)
+        assert torch.equal(o, o0) and torch.equal(lse, l0)
+
+
 def test_deterministic(cuda_device):
     q, k, v = make_qkv(2, 2, 300, 500, 128, "bf16", seed=21, device=cuda_device)
     o1, l1 = _run(q, k, v, 0.1)
