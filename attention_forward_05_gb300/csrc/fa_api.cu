@@ -335,15 +335,16 @@ int host_pipe(int dev, HostPipe** out) {
 // Chunks of fa_fwd_host, in key/value-head units.  The host link (about 200 GB/s each way) moves
 // the inputs slower than the forward consumes them, so what shows besides the copies is the first
 // chunk's copy in and the last chunk's compute and copy out.  A chunk launches `unit_ctas` CTAs per
-// unit; `wave` units fill the SMs' CTA slots once.  The last chunk is kHostLastWaves waves, the others
-// about kHostRestWaves each: small enough to start early and end soon, large enough that the forward
-// keeps up with the copies.  One wave each measured best (16 MB chunks, which left the d = 128
-// forward at under a wave per launch: 696 -> 757 TFLOP/s end to end; two waves: 752; three: 711).
-// Writes bounds[0 .. n] and returns n.
-constexpr int kHostRestWaves = 1, kHostLastWaves = 1;
+// unit; `wave` units fill the SMs' CTA slots once.  The chunks are about one wave each, the last
+// half a wave: small enough to start early and end soon, large enough that the forward keeps up with
+// the copies.  Measured end to end on both prefill problems: 16 MB chunks (the d = 128 forward at
+// under a wave per launch) 696 TFLOP/s; one-wave chunks 757-767; two-wave 752; three-wave 711; a
+// half-wave last chunk 777.  Writes bounds[0 .. n] and returns n.
+constexpr int kHostRestWaves = 1;
 int host_chunks(long long units, long long unit_ctas, long long slots, long long* bounds) {
   const long long wave = slots / unit_ctas > 1 ? slots / unit_ctas : 1;
-  const long long last = units < kHostLastWaves * wave ? units : kHostLastWaves * wave;
+  const long long half = wave / 2 > 1 ? wave / 2 : 1;
+  const long long last = units < half ? units : half;
   const long long rest = units - last;
   long long n_rest = 0;
   if (rest > 0) {

@@ -109,7 +109,7 @@ size_t fa_fwd_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d, int 
 /*
  * fa_fwd_host -- fa_fwd_ex (kv_splits = 0) on HOST-resident tensors: the library
  * copies q, k, v to the device, computes, and copies o and lse back, in chunks
- * of whole key/value heads (as many as fill the GPU's CTA slots once) so that the
+ * of whole key/value heads (about one wave of CTAs each) so that the
  * copies of one chunk overlap the compute of the previous one (copy-in and
  * copy-out on two internal streams, compute on `stream`, ordered by events).  The
  * exact attention computed is fa_fwd_ex's.
