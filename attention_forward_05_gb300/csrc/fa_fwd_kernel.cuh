@@ -29,8 +29,13 @@
 // Lazy rescale: a row's reference maximum m_ref only moves when the new
 // maximum exceeds it by more than tau (log2 units).  P = 2^(t - m_ref) then
 // stays below 2^tau, and since O and l share m_ref, O / l is unchanged; with
-// tau = 0 this is exactly the per-step correction of [T1] §2.3.
+// tau = 0 this is exactly the per-step correction of [T1] §2.3.  Once a row
+// has a reference maximum, tiles take fast paths that compute P against it
+// straight away: a row sum of P of at most 2^tau proves that no score moved
+// past m_ref + tau, so a row maximum is formed only where that test fails.
 #pragma once
+
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -470,20 +475,18 @@ __global__ void __maxnreg__(C::MAXREG)
       okw = __all_sync(0xffffffffu, okw);
       const int valid = row_lim - k_begin - j * C::BC - h * C::COLS;  // valid key columns here (may be <= 0)
       if constexpr (C::SPLIT == 1 && !C::TF32 && C::COLS <= 64) {
-        // Fast path for a full tile once every row of the warp has a reference maximum: P is
-        // computed against m_ref while the scores are still arriving, 32 columns at a time (the
-        // load of the next chunk overlaps the work on this one).  No row maximum is formed: the
-        // row sum bounds every P of the row, so a sum of at most 2^tau shows that no score moved
-        // past m_ref + tau.  Otherwise (rarely, and always when a maximum did move) the warp falls
-        // through to the general path below, which reloads S (not yet overwritten), takes the row
-        // maxima and rescales where needed.
+        // Fast path once every row of the warp has a reference maximum: P is computed against m_ref
+        // while the scores are still arriving, 32 columns at a time (the load of the next chunk
+        // overlaps the work on this one).  No row maximum is formed: the row sum bounds every P of
+        // the row, so a sum of at most 2^tau shows that no score moved past m_ref + tau.  Otherwise
+        // (rarely, and always when a maximum did move) the warp falls through to the general path
+        // below, which reloads S (not yet overwritten), takes the row maxima and rescales where
+        // needed.  A tile with masked columns (causal diagonal, ragged last tile) takes the masked
+        // copy of the path, whose P is 0 past each row's `valid` columns.
         // Only for 64-column tiles: with 128 columns the extra live registers spill and the
         // d = 128 kernel measured 25% slower.
-        if (__all_sync(0xffffffffu, valid >= C::COLS && m_ref != -INFINITY)) {
-          if (!okw) {
-            ok = false;
-            break;
-          }
+        auto fast = [&](auto masked) -> bool {
+          constexpr bool TAIL = decltype(masked)::value;
           tc_fence_after();
           const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
           uint32_t sc[2][32];
@@ -502,7 +505,11 @@ __global__ void __maxnreg__(C::MAXREG)
                                         negm2);
               float x0, x1;
               f2_unpack_f(x, x0, x1);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if constexpr (TAIL) {
+                if (cc * 32 + 2 * qc >= valid) p0 = 0.f;
+                if (cc * 32 + 2 * qc + 1 >= valid) p1 = 0.f;
+              }
               rs2[qc & 1] = f2_add(rs2[qc & 1], f2_pack(p0, p1));
               const int w = cc * 16 + qc;  // packed column of this pair
               pk[w / 32][w % 32] = pack_bf16x2(p0, p1);
@@ -516,16 +523,23 @@ __global__ void __maxnreg__(C::MAXREG)
           f2_unpack_f(rs2[0], r0, r1);
           f2_unpack_f(rs2[1], r2, r3);
           const float l_tile = (r0 + r1) + (r2 + r3);
-          if (__all_sync(0xffffffffu, l_tile <= p_lim)) {
+          if (!__all_sync(0xffffffffu, l_tile <= p_lim)) return false;
 #pragma unroll
-            for (int i = 0; i < C::PCOLS_W / 32; ++i) tmem_st32(tP + i * 32, pk[i]);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_pf(t));
-            l += l_tile;
-            continue;
+          for (int i = 0; i < C::PCOLS_W / 32; ++i) tmem_st32(tP + i * 32, pk[i]);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_pf(t));
+          l += l_tile;
+          return true;
+        };
+        if (__all_sync(0xffffffffu, m_ref != -INFINITY)) {
+          if (!okw) {
+            ok = false;
+            break;
           }
+          const bool full = __all_sync(0xffffffffu, valid >= C::COLS);
+          if (full ? fast(std::false_type{}) : fast(std::true_type{})) continue;
         }
       }
       if constexpr (C::PV2) {
