@@ -652,7 +652,7 @@ constexpr int kGqaTensorMinGroup = FA_GQA_TC_MIN_GROUP;
 // chunks in merge_order.  ws holds the fp32 states: O [splits][B*H][d], then (m, l) [splits][B*H].
 cudaError_t gqa_decode_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                int Hkv, int Nk, int d, int splits, int L, float scale, char* ws,
-                               const int* merge_order, int* err, cudaStream_t st) {
+                               const int* merge_order, int* err, int sms, cudaStream_t st) {
   const fa::FwdGeometry geo = fa::fwd_geometry_decode(d);
   const int G = H / Hkv, BHkv = B * Hkv;
   CUtensorMap tq, tk, tv;
@@ -683,7 +683,7 @@ cudaError_t gqa_decode_forward(const void* q, const void* k, const void* v, void
   a.tau = kLazyTau;
   a.fault = 0;
   a.stream = st;
-  cudaError_t e = (d == 64) ? fa::launch_fwd_decode_d64(a) : fa::launch_fwd_decode_d128(a);
+  cudaError_t e = fa::launch_fwd_decode(a, d, sms);
   if (e == cudaSuccess && splits > 1)
     e = fa::launch_fwd_merge(a.ws_o, a.ws_ml, o, lse, static_cast<long long>(rows), d, splits, 1, st, merge_order);
   return e;
@@ -713,9 +713,9 @@ int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, 
   const size_t need = fa_decode_workspace_bytes(B, H, d, splits);
   if (workspace && (!aligned16(workspace) || workspace_bytes < need)) return FA_ERR_INVALID_ARG;
 
-  int dev = 0;
+  int dev = 0, sms = 0;
   int* err = nullptr;
-  int rc = device_setup(&dev, &err);
+  int rc = device_setup(&dev, &err, &sms);
   if (rc != FA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   void* ws = workspace;
@@ -728,7 +728,7 @@ int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o, 
   cudaError_t e;
   if (H / Hkv >= kGqaTensorMinGroup && L % tile == 0 && static_cast<long long>(splits - 1) * L < Nk) {
     e = gqa_decode_forward(q, k, v, o, lse, B, H, Hkv, Nk, d, splits, L, scale, static_cast<char*>(ws), merge_order,
-                           err, st);
+                           err, sms, st);
     if (workspace == nullptr) {
       cudaError_t e2 = cudaFreeAsync(ws, st);
       if (e == cudaSuccess) e = e2;

@@ -87,8 +87,8 @@ cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a);
 cudaError_t launch_fwd_fp32_d64(const FwdLaunch& a);
 cudaError_t launch_fwd_fp32_d128(const FwdLaunch& a);
 // bf16 forward shaped for grouped-query decode (one query tile per CTA); see fa_fwd_decode.cu
-cudaError_t launch_fwd_decode_d64(const FwdLaunch& a);
-cudaError_t launch_fwd_decode_d128(const FwdLaunch& a);
+// `sms`: the device's SM count (picks the d = 64 configuration whose CTAs start in one wave, if any)
+cudaError_t launch_fwd_decode(const FwdLaunch& a, int d, int sms);
 FwdGeometry fwd_geometry_decode(int d);
 
 struct BwdLaunch {

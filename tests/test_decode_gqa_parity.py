@@ -40,6 +40,29 @@ def test_decode_gqa(cuda_device, d, H, Hkv, Nk, splits):
                  name=f"decode gqa d{d} H{H} Hkv{Hkv} Nk{Nk} s{splits}")
 
 
+def test_decode_gqa_one_wave_configuration(cuda_device):
+    """A tensor-core decode grid that only a fourth CTA per SM starts in one wave (one key/value head,
+    groups of 32; B from the SM count so that B*splits lies in (3*SMs, 4*SMs]) runs the 4-CTA d=64
+    configuration.  One query head of every batch (each reads every CTA of its batch), plus the first
+    and last, against the oracle."""
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    splits, H, Hkv, d = 16, 32, 1, 64
+    B = (4 * sms) // splits
+    assert 3 * sms < B * Hkv * splits <= 4 * sms
+    Nk = 2 * 64 * splits  # chunks of two whole key tiles
+    q, _, _ = make_qkv(B, H, 1, 1, d, "bf16", seed=2150, device=cuda_device)
+    _, k, v = make_qkv(B, Hkv, 1, Nk, d, "bf16", seed=2151, device=cuda_device)
+    order = merge_order(splits, 2152)
+    sc = 1 / math.sqrt(d)
+    o, lse = fa.fa_decode_splitkv_gqa(q, k, v, splits, scale=sc, with_lse=True,
+                                      merge_order=torch.as_tensor(order, device=cuda_device))
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    heads = sorted({0, B * H - 1, *[b * H + (7 * b) % H for b in range(B)]})
+    check_decode(q.reshape(B, H, d), _per_query_head(k, H), _per_query_head(v, H), o, lse, sc, splits, order,
+                 heads=heads, name=f"decode gqa one wave B{B} Nk{Nk}")
+
+
 def test_decode_gqa_matches_plain_decode_when_groups_are_one(cuda_device):
     """With Hkv = H the grouped kernel computes exactly what the per-head decode computes."""
     q, k, v = make_qkv(2, 4, 1, 777, 64, "bf16", seed=2300, device=cuda_device)
