@@ -342,8 +342,9 @@ __global__ void __maxnreg__(C::MAXREG)
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop, so descriptors and addresses are warp-uniform (uniform
-    // registers); one elected lane issues each tcgen05 instruction.  Waits are taken by all lanes
-    // and agreed with __all_sync.
+    // registers); one elected lane issues a tile's products and commits of a step in one region
+    // (issue_qk and issue_pv are called from that lane; electing per instruction measured 2-5%
+    // slower at d=64).  Waits are taken by all lanes and agreed with __all_sync.
     {
       auto wait_all = [&](uint32_t bar, uint32_t parity, int where) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, p.err, where));
@@ -366,7 +367,7 @@ __global__ void __maxnreg__(C::MAXREG)
           const int e = kk * C::MMA_K;  // element offset along d: 128-byte segment, then 32-byte step inside it
           const uint32_t oq = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * C::ESZ) >> 4;
           const uint32_t ok_ = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * C::ESZ) >> 4;
-          if (elect_one()) mma_ss<C::TF32>(d_tmem, qa + oq, kb + ok_, idesc_qk, kk > 0);
+          mma_ss<C::TF32>(d_tmem, qa + oq, kb + ok_, idesc_qk, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc, int kk0 = 0, int kk1 = C::BC / C::MMA_K) {
@@ -382,8 +383,7 @@ __global__ void __maxnreg__(C::MAXREG)
           } else {  // [Bc keys][D]: MN-major, 8-key groups 1024 B apart, 64-column segments LBO apart
             ov = (kk * C::MMA_K * 128) >> 4;
           }
-          if (elect_one())
-            mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_K, vb + ov, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          mma_ts<C::TF32>(d_tmem, a_tmem + kk * C::P_COLS_PER_K, vb + ov, idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
       auto commit = [&](uint32_t bar) {
@@ -393,14 +393,17 @@ __global__ void __maxnreg__(C::MAXREG)
       bool ok = T > 0 && wait_all(bar_q, 0, W_Q) && wait_all(bar_kf(0), 0, W_KF);
       if (ok) {
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int t = 0; t < C::NQT; ++t) {
-          if (tile_steps(t) > 0) {
-            issue_qk(t, 0);
-            commit(bar_sf(t));
+          for (int t = 0; t < C::NQT; ++t) {
+            if (tile_steps(t) > 0) {
+              issue_qk(t, 0);
+              mma_commit(bar_sf(t));
+            }
           }
+          mma_commit(bar_ke(0));
         }
-        commit(bar_ke(0));
+        __syncwarp();
       }
       for (int j = 0; ok && j < T; ++j) {
         const int s = j % C::STAGES;
@@ -420,26 +423,33 @@ __global__ void __maxnreg__(C::MAXREG)
               ok = wait_all(bar_ph(t), j & 1, W_PF);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(t, s, j > 0, 0, C::BC / C::MMA_K / 2);
+              if (elect_one()) issue_pv(t, s, j > 0, 0, C::BC / C::MMA_K / 2);
+              __syncwarp();
             }
             ok = wait_all(bar_pf(t), j & 1, W_PF);
             if (!ok) break;
             tc_fence_after();
-            if constexpr (C::PV2)
-              issue_pv(t, s, true, C::BC / C::MMA_K / 2, C::BC / C::MMA_K);
-            else
-              issue_pv(t, s, j > 0);
           }
-          if (t == C::NQT - 1) commit(bar_ve(s));
-          if (j < Tt) {
-            if (j1 < Tt) {
-              issue_qk(t, s1);
-              commit(bar_sf(t));
-            } else {
-              commit(bar_od(t));
+          // one elected lane issues the step's products and commits for this tile in one go
+          if (elect_one()) {
+            if (j < Tt) {
+              if constexpr (C::PV2)
+                issue_pv(t, s, true, C::BC / C::MMA_K / 2, C::BC / C::MMA_K);
+              else
+                issue_pv(t, s, j > 0);
             }
+            if (t == C::NQT - 1) mma_commit(bar_ve(s));
+            if (j < Tt) {
+              if (j1 < Tt) {
+                issue_qk(t, s1);
+                mma_commit(bar_sf(t));
+              } else {
+                mma_commit(bar_od(t));
+              }
+            }
+            if (t == C::NQT - 1 && j1 < T) mma_commit(bar_ke(s1));
           }
-          if (t == C::NQT - 1 && j1 < T) commit(bar_ke(s1));
+          __syncwarp();
         }
       }
       // Drain: all MMAs issued above complete before tensor memory is freed.
