@@ -200,6 +200,16 @@ __device__ __forceinline__ void softmax_p_tf32(uint32_t (&sr)[NCOL / 32][32], ui
   }
 }
 
+// Warp-collective: r[0..15] to 16 consecutive 32-bit TMEM columns of this warp's lanes.
+__device__ __forceinline__ void tmem_st16_lo(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 template <class C>
 __global__ void __maxnreg__(C::MAXREG)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -608,10 +618,31 @@ __global__ void __maxnreg__(C::MAXREG)
           }
         }
       }
-      uint32_t sr[C::COLS / 32][32];
+      // 64-column bf16 tiles: the general path works on one 32-column chunk at a time (the maximum, then
+      // P chunk by chunk), which halves the registers it holds; P and the row sum come out the same.
+      constexpr bool CHUNKED = !C::TF32 && !C::PV2 && C::SPLIT == 1 && C::COLS == 64;
+      uint32_t sr[CHUNKED ? 1 : C::COLS / 32][32];
       float m_part = -INFINITY;
-      {  // loaded even when the wait gave up (then the values are stale and unused): a conditional
-         // load would keep the row in local memory
+      if constexpr (CHUNKED) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          tmem_ld32(tS + cc * 32, sr[0]);
+          tmem_wait_ld();
+          reg_fence(sr[0]);
+          const int vc = valid - cc * 32;
+          if (vc > 0) {
+            if (vc < 32) {  // ragged: repeat the chunk's column 0 so max/min ignore the pad
+              const uint32_t s0 = sr[0][0];
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (e >= vc) sr[0][e] = s0;
+            }
+            m_part = fmaxf(m_part, (c >= 0.f ? row_extreme<32, true>(sr) : row_extreme<32, false>(sr)) * c);
+          }
+        }
+      } else {  // loaded even when the wait gave up (then the values are stale and unused): a conditional
+                // load would keep the row in local memory
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < C::COLS / 32; ++i) tmem_ld32(tS + i * 32, sr[i]);
@@ -699,6 +730,29 @@ __global__ void __maxnreg__(C::MAXREG)
         else softmax_p_bf16<HC, true>(sr_b, pk_b, c2, negm2, valid - HC, rs2);
 #pragma unroll
         for (int i = 0; i < HC / 64; ++i) tmem_st32(tP + (HC / 64 + i) * 32, pk_b[i]);
+      } else if constexpr (CHUNKED) {
+        // chunk cc's 16 packed P columns go over S columns 16cc .. 16cc+15, which hold chunk 0 (already read)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          tmem_ld32(tS + cc * 32, sr[0]);
+          tmem_wait_ld();
+          reg_fence(sr[0]);
+          const int vc = valid - cc * 32;
+          uint32_t pk[32];
+#pragma unroll
+          for (int qc = 0; qc < 16; ++qc) {
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[0][2 * qc]), __uint_as_float(sr[0][2 * qc + 1])), c2,
+                                      negm2);
+            float x0, x1;
+            f2_unpack_f(x, x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (2 * qc >= vc) p0 = 0.f;
+            if (2 * qc + 1 >= vc) p1 = 0.f;
+            rs2[qc & 1] = f2_add(rs2[qc & 1], f2_pack(p0, p1));  // the same accumulator order as one pass
+            pk[qc] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16_lo(tP + cc * 16, pk);
+        }
       } else {
         uint32_t pk[C::PCOLS_W / 32][32];
         if (valid >= C::COLS) softmax_p_bf16<C::COLS, false>(sr, pk, c2, negm2, valid, rs2);
