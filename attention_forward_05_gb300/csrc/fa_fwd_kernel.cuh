@@ -122,6 +122,7 @@ struct FwdParams {
   int causal;           // 1: query row i sees keys j <= i + causal_off only
   int causal_off;       // Nk - Nq (mask aligned to the bottom-right corner)
   float c, tau;
+  float p_lim;          // 2^tau: largest row sum of P that proves no maximum moved past m_ref + tau
   int fault;
 };
 
@@ -488,7 +489,7 @@ __global__ void __maxnreg__(C::MAXREG)
     float l = 0.f;
     bool ok = true;
     const uint64_t c2 = f2_pack(c, c);
-    const float p_lim = exp2f(p.tau);  // largest row sum of P that proves no maximum moved past m_ref + tau
+    const float& p_lim = p.p_lim;  // read from the kernel parameters where used (no register held)
     const int Tt = tile_steps(t);      // key tiles of this query tile
     for (int j = 0; j < Tt; ++j) {
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
@@ -909,6 +910,7 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   if (a.causal && (a.Nq > a.Nk || a.n_split < 1)) return cudaErrorInvalidValue;
   p.c = a.c;
   p.tau = a.tau;
+  p.p_lim = exp2f(a.tau);
   p.fault = a.fault;
   if (a.n_split < 1 || a.kv_per_split < C::BC || a.kv_per_split % C::BC != 0 ||
       static_cast<long long>(a.n_split - 1) * a.kv_per_split >= a.Nk)
