@@ -70,6 +70,18 @@ int device_setup(int* dev_out, int** err_out, int* sms_out = nullptr) {
   return FA_OK;
 }
 
+}  // namespace
+
+namespace fa {
+int current_device_status() {
+  int dev = 0;
+  int* err = nullptr;
+  return device_setup(&dev, &err);
+}
+}  // namespace fa
+
+namespace {
+
 // 3-D tiled map over a contiguous [BH, rows, inner] tensor: dims (inner, rows, BH),
 // box (box_cols, box_rows, 1), 128-byte swizzle, out-of-bounds elements read as zero.
 int encode_map(CUtensorMap* map, const void* base, bool bf16, int BH, int rows, int inner, int box_cols,
@@ -309,7 +321,8 @@ struct HostPipe {
   std::mutex mu;
   bool ready = false;
   cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[kHostMaxChunks] = {}, ev_done[kHostMaxChunks] = {};
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in_end = nullptr, ev_in[kHostMaxChunks] = {},
+              ev_done[kHostMaxChunks] = {};
 };
 HostPipe g_pipe[kMaxDevices];
 
@@ -320,7 +333,8 @@ int host_pipe(int dev, HostPipe** out) {
     if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
         (e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&hp.ev_start, cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&hp.ev_end, cudaEventDisableTiming)) != cudaSuccess)
+        (e = cudaEventCreateWithFlags(&hp.ev_end, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.ev_in_end, cudaEventDisableTiming)) != cudaSuccess)
       return cuda_fail(e);
     for (int i = 0; i < kHostMaxChunks; ++i)
       if ((e = cudaEventCreateWithFlags(&hp.ev_in[i], cudaEventDisableTiming)) != cudaSuccess ||
@@ -460,9 +474,13 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
                                     hp->s_out)) != cudaSuccess)
       break;
   }
-  // the caller's stream waits for the last copy out; later work on it sees finished host buffers
+  // The caller's stream waits for the last copy out (later work on it sees finished host buffers) and
+  // for every copy in: after an error part-way through a chunk, copies already queued on s_in may not
+  // yet be covered by an ev_in event, and the workspace must outlive them.
   cudaError_t e2 = cudaEventRecord(hp->ev_end, hp->s_out);
   if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, hp->ev_end, 0);
+  if (e2 == cudaSuccess) e2 = cudaEventRecord(hp->ev_in_end, hp->s_in);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, hp->ev_in_end, 0);
   if (e == cudaSuccess) e = e2;
   if (own_ws) {
     e2 = cudaFreeAsync(ws, st);

@@ -75,6 +75,9 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k, const voi
   if (BH * static_cast<long long>(Nk) * d > (1LL << 40)) return FA_ERR_INVALID_ARG;
   if (fa_decode_workspace_bytes(B, H, d, splits) > kScratchBytes) return FA_ERR_UNSUPPORTED;
 
+  // the same device check as every other entry point: sm_103 only, FA_ERR_UNSUPPORTED elsewhere
+  const int dev_status = fa::current_device_status();
+  if (dev_status != FA_OK) return dev_status;
   void* ws = nullptr;
   if (scratch_address(&ws) != cudaSuccess) return FA_ERR_CUDA;
   fa::DecodeLaunch a;

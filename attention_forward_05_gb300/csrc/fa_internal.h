@@ -38,6 +38,11 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, int thread
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// The C ABI's per-device check for the current device: FA_OK on an sm_103 GPU (after fetching the
+// library's device error word), FA_ERR_UNSUPPORTED on any other device, FA_ERR_CUDA when a runtime
+// call fails.  Allocates nothing.
+int current_device_status();
+
 struct FwdLaunch {
   const CUtensorMap* tm_q;  // 3-D maps over [B*H, N, d] (innermost d), 128-byte swizzle
   const CUtensorMap* tm_k;

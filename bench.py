@@ -34,6 +34,12 @@ WORKLOAD = ("bf16 prefill B=4 H=16 N=4096 d=64 + B=2 H=16 N=8192 d=128 (Q,K x3);
             "split-KV decode B=32 H=32 Nk=32768 d=64 splits=16 (seeded merge order)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PREFILL = ("mh_prefill", "peaked_d128")
+# fp32-in configurations (products on the tensor cores' tf32 path), timed beside the step but not part
+# of `value`; their roofline is the tf32 dense peak: the measured bf16 burst peak scaled by the nominal
+# dense tf32 / bf16 ratio of the part (1.1 / 2.25 PFLOP/s).
+PREFILL_FP32 = ("tiny_fp32", "long_fp32")
+TF32_PER_BF16 = 1.1 / 2.25
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 
 
 def parse_args():
@@ -227,6 +233,58 @@ def oracle_decode_sample(oracle, q, k, v, splits, scale, order, seconds):
             return nbytes, el, calls
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            key, val = (x.strip() for x in line.split(":", 1))
+            fields.setdefault(key.lower(), val)
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu implementer" in fields:  # Arm: implementer / part codes
+        return f"Arm implementer {fields['cpu implementer']} part {fields.get('cpu part', '?')}"
+    return "unknown"
+
+
+class OneCore:
+    """Pins the calling thread to one allowed core for the oracle timing (process-local; restores the
+    previous affinity on exit) and describes the host for the cpu_baseline record."""
+
+    def __enter__(self):
+        self.old = None
+        self.core = None
+        if hasattr(os, "sched_setaffinity"):
+            try:
+                self.old = os.sched_getaffinity(0)
+                self.core = max(self.old)
+                os.sched_setaffinity(0, {self.core})
+            except OSError:
+                self.old = self.core = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.old is not None:
+            os.sched_setaffinity(0, self.old)
+        return False
+
+    def record(self) -> dict:
+        return {"host_cpus": os.cpu_count(), "cpu_model": cpu_model(),
+                "pinned_core": self.core, "threads": 1}
+
+
 def host_inputs(name):
     """CPU copies of a workload's inputs (heads generated on demand are enough for the oracle samples)."""
     from attention_forward_05_gb300.inputs import WORKLOADS, make_qkv
@@ -245,12 +303,13 @@ def run_reference(args):
     w, (q, k, v) = host_inputs("mh_prefill")
     total_flops, total_t = 0, 0.0
     per_step = []
-    for i in range(args.warmup + args.steps):
-        f, t, _ = oracle_prefill_sample(oracle, q, k, v, w.scale, seconds=0.0, rows_per_call=64, min_calls=2)
-        if i >= args.warmup:
-            total_flops += f
-            total_t += t
-            per_step.append(t)
+    with OneCore() as pin:
+        for i in range(args.warmup + args.steps):
+            f, t, _ = oracle_prefill_sample(oracle, q, k, v, w.scale, seconds=0.0, rows_per_call=64, min_calls=2)
+            if i >= args.warmup:
+                total_flops += f
+                total_t += t
+                per_step.append(t)
     value = total_flops / total_t / 1e12
     cores = 1
     sample = f"{2 * 64} query rows of one mh_prefill head (Nk=4096, d=64) per step, float64 C, 1 thread"
@@ -259,7 +318,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(per_step),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample": sample},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         **pin.record()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -275,16 +335,19 @@ def cpu_baseline(seconds):
     from attention_forward_05_gb300.inputs import merge_order
     oracle.build()
     w, (q, k, v) = host_inputs("mh_prefill")
-    f, t, calls = oracle_prefill_sample(oracle, q, k, v, w.scale, seconds=seconds * 0.7)
-    pre = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-           "sample": f"{calls} x 64 query rows of mh_prefill heads (Nk=4096, d=64), float64 C, 1 thread, {t:.1f} s"}
     from attention_forward_05_gb300.inputs import WORKLOADS, make_qkv
     wd = WORKLOADS["decode"]
     qd, kd, vd = make_qkv(1, 2, 1, wd.Nk, wd.d, "bf16", wd.seed, device="cpu")
     order = merge_order(wd.splits, wd.order_seed)
-    nb, td, cd = oracle_decode_sample(oracle, qd, kd, vd, wd.splits, wd.scale, order, seconds * 0.3)
+    with OneCore() as pin:
+        f, t, calls = oracle_prefill_sample(oracle, q, k, v, w.scale, seconds=seconds * 0.7)
+        nb, td, cd = oracle_decode_sample(oracle, qd, kd, vd, wd.splits, wd.scale, order, seconds * 0.3)
+    pre = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+           "sample": f"{calls} x 64 query rows of mh_prefill heads (Nk=4096, d=64), float64 C, 1 thread, {t:.1f} s",
+           **pin.record()}
     dec = {"value": nb / td / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": f"{cd} decode heads (Nk=32768, d=64, 16 splits), float64 C, 1 thread, {td:.1f} s"}
+           "sample": f"{cd} decode heads (Nk=32768, d=64, 16 splits), float64 C, 1 thread, {td:.1f} s",
+           **pin.record()}
     return pre, dec
 
 
@@ -406,6 +469,7 @@ def run_gpu(args):
         parts[n] = {"ms": ms, "tflops": ach, "frac": ach / peaks["bf16_tflops"],
                     "flops_per_launch": pre_flops[n]}
     dom = max(parts, key=lambda n: parts[n]["ms"])
+    parts.update(measure_fp32(fa, torch, accounting, dev, stream, peaks["bf16_tflops"] * TF32_PER_BF16, peak_src))
     ms_dec = statistics.mean(dec_ms)
     roof = {"bound": "tensor", "kernel": f"fa_fwd_kernel bf16 ({dom})",
             "achieved": parts[dom]["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -441,6 +505,42 @@ def run_gpu(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def measure_fp32(fa, torch, accounting, dev, stream, tf32_peak, peak_src, launches=50):
+    """The fp32-in workloads through fa_fwd as a user calls it (automatic key splits): each launch
+    group (prep, forward, merge) timed alone with CUDA events on `stream`, after 3 warm-up calls, with
+    L2 flushed before every timed launch (the inputs are far smaller than L2)."""
+    from attention_forward_05_gb300.inputs import WORKLOADS, workload_inputs
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {}
+    for name in PREFILL_FP32:
+        w = WORKLOADS[name]
+        q, k, v = workload_inputs(w, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.Nq), device=dev, dtype=torch.float32)
+        call = lambda: fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse, stream=stream)
+        for _ in range(3):
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                flush.fill_(1)
+                a.record(stream)
+                call()
+                b.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        fl = accounting.fwd_flops(w.B, w.H, w.Nq, w.Nk, w.d)
+        ach = fl / (ms / 1e3) / 1e12
+        out[name] = {"ms": ms, "tflops": ach, "frac": ach / tf32_peak, "flops_per_launch": fl,
+                     "in_value": False, "dtype": "fp32 in, tf32 products", "peak": tf32_peak,
+                     "peak_source": f"{peak_src} bf16 burst x 1.1/2.25 (nominal dense tf32/bf16 ratio)",
+                     "l2": "flushed before every timed launch", "launches": launches}
+        del q, k, v, o, lse
+    if fa.fa_check_device_error() != fa.FA_OK:
+        raise RuntimeError("device timeout in the fp32 measurements")
+    return out
 
 
 def measure_extras(fa, torch, accounting, dev, stream, launches=20, hbm_gbs=None):

@@ -7,6 +7,7 @@
  *   [T1] "FlashAttention 简化版：Tiling + Online Softmax" (forceinjection.github.io)
  *   [T2] "Flash Attention 代码填空 (Level 2-3)" (boots-coder.github.io, LLM-101-CN)
  *   [T3] "CS349E 第 11 讲 01_online_softmax.py" (semidirectx.com)
+ *   [T4] "从零手写 FlashAttention（PyTorch实现 + 原理推导）" (mokono.cn)
  *
  * Conventions shared by every entry point
  *   - Tensors are contiguous row-major [B, H, N, d] (d fastest).  Decode q and
@@ -233,7 +234,8 @@ int fa_decode_splitkv_gqa(const void* q, const void* k, const void* v, void* o,
  *   every GPU that loads the library holds until the process exits.  The call
  *   allocates and frees nothing.
  *   - FA_ERR_UNSUPPORTED if fa_decode_workspace_bytes(B, H, d, splits) exceeds
- *     FA_DECODE_NOALLOC_SCRATCH_BYTES (nothing is launched).
+ *     FA_DECODE_NOALLOC_SCRATCH_BYTES, or if the current device is not an
+ *     sm_103 GPU (nothing is launched in either case).
  *   - All calls share the array: calls whose kernels may overlap on the GPU
  *     (unordered streams) race and must be ordered by the caller.  The array
  *     keeps the previous call's contents; nothing needs clearing, since every

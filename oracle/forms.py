@@ -62,44 +62,57 @@ def softmax_online(x: np.ndarray) -> np.ndarray:
 # one query row ([T3] demo 1)
 # ----------------------------------------------------------------------------
 
+def _key_ranges(n: int, width: int) -> list[tuple[int, int]]:
+    """Half-open key ranges [lo, hi) of `width` keys (the last one shorter) covering 0 .. n."""
+    return [(lo, min(n, lo + width)) for lo in range(0, n, width)]
+
+
+def _block_scores(q: np.ndarray, K: np.ndarray, lo: int, hi: int, scale: float) -> np.ndarray:
+    """Scaled scores of one query against keys lo .. hi-1."""
+    return scale * (K[lo:hi] @ q)
+
+
 def attn_row_2pass(q: np.ndarray, K: np.ndarray, V: np.ndarray, block: int, scale: float) -> np.ndarray:
-    """Two passes over K: online (m, l) by blocks, then recomputed scores weight V ([T3] attn_row_2pass)."""
-    n = K.shape[0]
-    m, l = -math.inf, 0.0
-    for a in range(0, n, block):
-        s = (K[a:a + block] @ q) * scale
-        m_new = max(m, float(s.max()))
-        l = l * math.exp(m - m_new) + float(np.exp(s - m_new).sum())
-        m = m_new
-    out = np.zeros(V.shape[1])
-    for a in range(0, n, block):
-        s = (K[a:a + block] @ q) * scale
-        out += (np.exp(s - m) / l) @ V[a:a + block]
-    return out
+    """Two sweeps over the keys of one query ([T3] demo 1, the two-pass form).
+
+    The first sweep only gathers the softmax statistics block by block (running maximum, and the
+    running sum re-based whenever the maximum moves); the second sweep recomputes each block's
+    scores and accumulates their normalised weights times V.
+    """
+    ranges = _key_ranges(K.shape[0], block)
+    stat_m, stat_l = -math.inf, 0.0
+    for lo, hi in ranges:
+        s = _block_scores(q, K, lo, hi, scale)
+        top = max(stat_m, float(np.max(s)))
+        stat_l = stat_l * math.exp(stat_m - top) + float(np.sum(np.exp(s - top)))
+        stat_m = top
+    weighted = [np.exp(_block_scores(q, K, lo, hi, scale) - stat_m) @ V[lo:hi] for lo, hi in ranges]
+    return np.sum(weighted, axis=0) / stat_l
 
 
 def attn_row_1pass(q: np.ndarray, K: np.ndarray, V: np.ndarray, block: int, scale: float,
                    trace: list | None = None) -> np.ndarray:
-    """One pass over K and V with running (m, l, acc) and a final acc / l ([T3] attn_row_1pass).
+    """One sweep over keys and values of one query ([T3] demo 1, the one-pass form).
 
-    Per block: m_new = max(m, block max), alpha = exp(m - m_new),
-    l <- alpha l + sum exp(s - m_new), acc <- alpha acc + exp(s - m_new) V_block.
-    If `trace` is a list, (block index, block max, m_new, alpha, l) is appended per block.
+    The state (m, l, o) is the running maximum, the running sum and the unnormalised output.  A
+    block with scores s moves the maximum to m' = max(m, max s); the old sum and output are
+    re-based by alpha = exp(m - m') before the block's weights exp(s - m') are added.  The
+    division by l comes once, after the last block.  If `trace` is a list, one record
+    (block index, block max, m', alpha, l) is appended per block.
     """
-    n = K.shape[0]
-    m, l = -math.inf, 0.0
-    acc = np.zeros(V.shape[1])
-    for a in range(0, n, block):
-        s = (K[a:a + block] @ q) * scale
-        m_new = max(m, float(s.max()))
-        alpha = math.exp(m - m_new)
-        p = np.exp(s - m_new)
-        l = alpha * l + float(p.sum())
-        acc = alpha * acc + p @ V[a:a + block]
+    state_m, state_l, state_o = -math.inf, 0.0, np.zeros(V.shape[1])
+    for idx, (lo, hi) in enumerate(_key_ranges(K.shape[0], block)):
+        s = _block_scores(q, K, lo, hi, scale)
+        blk_max = float(np.max(s))
+        moved = max(state_m, blk_max)
+        alpha = math.exp(state_m - moved)
+        w = np.exp(s - moved)
+        state_o = state_o * alpha + w @ V[lo:hi]
+        state_l = state_l * alpha + float(np.sum(w))
+        state_m = moved
         if trace is not None:
-            trace.append((a // block, float(s.max()), m_new, alpha, l))
-        m = m_new
-    return acc / l
+            trace.append((idx, blk_max, moved, alpha, state_l))
+    return state_o / state_l
 
 
 # ----------------------------------------------------------------------------

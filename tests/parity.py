@@ -9,17 +9,28 @@ fp32 m, l and accumulators):
   LSE (both):                   max |dLSE| <= 1e-3
 The oracle always runs on the exact bytes the GPU saw (bf16 up-cast exactly).
 
-Two readings make these bounds attainable at the edges, both derived from the
-arithmetic rather than tuned:
-  * bf16 output: O is stored in bf16, so even a correctly rounded output is up
-    to half a bf16 step from the exact value (0.0156 once |O| >= 4, which
-    happens with peaked scores where O is close to a single V row).  The
-    1.5e-2 bound is applied to the error beyond that half step.
-  * fp32 inputs: Q and K are rounded to tf32 (unit roundoff u = 2^-11) before
-    the tensor core multiplies them, so a score can be off by up to
-    2u |scale| sum_i |q_i k_i|; LSE is a softmax-weighted mean of scores, so
-    its error is below the largest such score bound.  With few keys nothing
-    averages out, and the LSE bound is max(1e-3, that bound).
+How the bf16 bound is applied.  O is stored in bf16, so even a correctly
+rounded output sits up to half a bf16 step from the exact value: 0.0156 once
+|O| >= 4, which is more than the 1.5e-2 bound itself (peaked scores put O close
+to a single V row, and V rows reach |v| > 4).  Every bf16 check therefore
+asserts two things, and reports the raw max |dO| beside them:
+  * direct: |O_gpu - RNE_bf16(O_oracle)| <= 1.5e-2, the GPU's bf16 output
+    against the oracle rounded to bf16 the way the kernel rounds.  Where one
+    bf16 step is larger than 1.5e-2 (|O| >= 2) an output one step away from
+    RNE_bf16(O_oracle) still passes: a kernel error of any size can put the
+    two values on either side of a rounding boundary.
+  * beyond the format: |O_gpu - O_oracle| - half_step(O_oracle) <= 1.5e-2.
+
+How the fp32 LSE bound is applied.  Q and K are rounded to tf32 (unit
+roundoff u = 2^-11) before the tensor core multiplies them, so one score is
+off by about u |scale| sqrt(2/3 sum_i (q_i k_i)^2) (4e-4 for N(0,1) inputs at
+d = 64 or 128 with scale 1/sqrt(d); at most 2u |scale| sum_i |q_i k_i|).  LSE
+is a softmax-weighted mean of the scores, so these errors average out over the
+keys a row sees: with n keys of similar weight the LSE error is about
+4e-4 sqrt(e / n), and a bound of 1e-3 holds with a wide margin from n = 16 on.
+Rows that see fewer than 16 keys (single-key shapes, the first rows under a
+causal mask) are held to max(1e-3, the worst-case score bound); every other
+row is held to 1e-3.
 """
 from __future__ import annotations
 
@@ -38,13 +49,16 @@ def dtype_name(t: torch.Tensor) -> str:
     return "bf16" if t.dtype == torch.bfloat16 else "fp32"
 
 
-def sample_rows(Nq: int, n_random: int, seed: int, tile: int = 128, n_tiles: int = 12) -> np.ndarray:
-    """Seeded rows: first and last row of the first two, the last, and `n_tiles` random 128-row
-    query tiles, plus `n_random` random rows."""
+# Rows that see fewer keys than this are given the tf32 worst-case LSE bound (module docstring).
+FEW_KEYS = 16
+
+
+def sample_rows(Nq: int, n_random: int, seed: int, tile: int = 128) -> np.ndarray:
+    """Seeded rows: the first and last row of every 128-row query tile (so every tile and CTA
+    boundary), plus `n_random` random rows."""
     rng = np.random.default_rng(seed)
     n_t = (Nq + tile - 1) // tile
-    tiles = {0, min(1, n_t - 1), n_t - 1}
-    tiles.update(rng.choice(n_t, size=min(n_tiles, n_t), replace=False).tolist())
+    tiles = range(n_t)
     rows = set()
     for t in tiles:
         rows.add(t * tile)
@@ -65,23 +79,58 @@ def check_fwd(q, k, v, o, lse, scale: float, rows=None, name: str = "", causal: 
     ref_o, ref_lse = oracle.attention(qs, k, v, scale, causal=causal, rows=rows, nq_total=q.shape[2])
     got = og.float().cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all(), f"{name}: non-finite output"
-    err = np.abs(got - ref_o)
-    res = dict(max_o=float(err.max()), mean_o=float(err.mean()))
     tol = TOL[dt]
-    beyond = err - bf16_half_step(ref_o) if dt == "bf16" else err
-    res["max_o_beyond_format"] = float(beyond.max())
-    assert res["max_o_beyond_format"] <= tol["max_o"], \
-        f"{name}: max|dO| {res['max_o']:.3e} ({res['max_o_beyond_format']:.3e} beyond bf16 rounding) > {tol['max_o']}"
-    if tol["mean_o"] is not None:
-        assert res["mean_o"] <= tol["mean_o"], f"{name}: mean|dO| {res['mean_o']:.3e} > {tol['mean_o']}"
+    if dt == "bf16":
+        res = check_bf16_output(got, ref_o, name)
+    else:
+        err = np.abs(got - ref_o)
+        res = dict(max_o=float(err.max()), mean_o=float(err.mean()))
+        assert res["max_o"] <= tol["max_o"], f"{name}: max|dO| {res['max_o']:.3e} > {tol['max_o']}"
     if lg is not None:
         le = np.abs(lg.cpu().numpy().astype(np.float64) - ref_lse)
         res["lse"] = float(le.max())
         lse_tol = np.full(le.shape, tol["lse"])
         if dt == "fp32":
-            lse_tol = np.maximum(lse_tol, tf32_score_bound(qs, k, scale))
+            row_ids = np.arange(q.shape[2]) if rows is None else np.asarray(rows)
+            nk = k.shape[2]
+            seen = np.minimum(nk, row_ids + 1 + nk - q.shape[2]) if causal else np.full(row_ids.shape, nk)
+            few = (seen < FEW_KEYS)[None, None, :]
+            lse_tol = np.where(few, np.maximum(lse_tol, tf32_score_bound(qs, k, scale)), lse_tol)
+            res["lse_rows_few_keys"] = float(few.sum())
+            rest = le[np.broadcast_to(~few, le.shape)]
+            if rest.size:
+                res["lse_many_keys"] = float(rest.max())
         assert (le <= lse_tol).all(), f"{name}: max|dLSE| {res['lse']:.3e} above its bound"
     print(f"[parity] {name}: " + " ".join(f"{k}={v:.3e}" for k, v in res.items()))
+    return res
+
+
+def rne_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 values rounded to the nearest bf16 value (8 significant bits), ties to even."""
+    mant, ex = np.frexp(x)  # x = mant * 2^ex with 0.5 <= |mant| < 1
+    step = np.exp2(np.maximum(ex, -125) - 8.0)
+    return np.round(x / step) * step  # np.round rounds halves to even
+
+
+def bf16_step(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |x|: 2^(floor(log2|x|) - 7)."""
+    return 2.0 * bf16_half_step(x)
+
+
+def check_bf16_output(got: np.ndarray, ref: np.ndarray, name: str) -> dict:
+    """bf16 outputs against float64 oracle values: the direct and the beyond-format bound of the module
+    docstring, and the mean bound; returns the raw and direct figures."""
+    tol = TOL["bf16"]
+    err = np.abs(got - ref)
+    direct = np.abs(got - rne_bf16(ref))
+    beyond = err - bf16_half_step(ref)
+    res = dict(max_o=float(err.max()), mean_o=float(err.mean()), max_o_vs_rne=float(direct.max()),
+               max_o_beyond_format=float(beyond.max()))
+    ok_direct = direct <= np.maximum(tol["max_o"], bf16_step(ref) * 1.0000001)
+    assert ok_direct.all(), f"{name}: |O - RNE(O_ref)| up to {res['max_o_vs_rne']:.3e} above {tol['max_o']}"
+    assert res["max_o_beyond_format"] <= tol["max_o"], \
+        f"{name}: max|dO| {res['max_o']:.3e} ({res['max_o_beyond_format']:.3e} beyond bf16 rounding) > {tol['max_o']}"
+    assert res["mean_o"] <= tol["mean_o"], f"{name}: mean|dO| {res['mean_o']:.3e} > {tol['mean_o']}"
     return res
 
 
@@ -118,12 +167,8 @@ def check_decode(q, k, v, o, lse, scale: float, splits: int, order=None, heads=N
     ref_o, ref_lse = oracle.decode_splitkv(qf, kf, vf, splits, scale, order)
     got = of.float().cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all(), f"{name}: non-finite output"
-    err = np.abs(got - ref_o)
-    res = dict(max_o=float(err.max()), mean_o=float(err.mean()))
     tol = TOL["bf16"]
-    res["max_o_beyond_format"] = float((err - bf16_half_step(ref_o)).max())
-    assert res["max_o_beyond_format"] <= tol["max_o"], f"{name}: max|dO| {res['max_o']:.3e}"
-    assert res["mean_o"] <= tol["mean_o"], f"{name}: mean|dO| {res['mean_o']:.3e}"
+    res = check_bf16_output(got, ref_o, name)
     if lf is not None:
         le = np.abs(lf.cpu().numpy().astype(np.float64) - ref_lse)
         res["lse"] = float(le.max())
