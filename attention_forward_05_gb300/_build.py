@@ -46,7 +46,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     FA_PTXAS_VERBOSE=1 in the environment adds ``-Xptxas -v`` and keeps its
     register / spill report in _build/ptxas.log.  FA_NVCC_EXTRA adds compiler
-    flags (e.g. tile-configuration definitions for tuning builds); a build
+    flags (for experiments outside the library's own configuration); a build
     with different extra flags is always redone.
     """
     extra = os.environ.get("FA_NVCC_EXTRA", "").split()

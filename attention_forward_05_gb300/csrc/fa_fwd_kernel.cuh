@@ -158,18 +158,10 @@ __device__ __forceinline__ void softmax_p_bf16(const uint32_t (&sr)[NCOL / 32][3
 #pragma unroll
   for (int qc = 0; qc < NCOL / 2; ++qc) {
     const int e0 = 2 * qc;
-#ifdef FA_SOFTMAX_SCALAR  // tuning build: scalar FFMA instead of the packed pair
-    float c_, nm_, d_;
-    f2_unpack_f(c2, c_, d_);
-    f2_unpack_f(negm2, nm_, d_);
-    const float x0 = fmaf(__uint_as_float(sr[e0 / 32][e0 % 32]), c_, nm_);
-    const float x1 = fmaf(__uint_as_float(sr[e0 / 32][e0 % 32 + 1]), c_, nm_);
-#else
     const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[e0 / 32][e0 % 32]), __uint_as_float(sr[e0 / 32][e0 % 32 + 1])),
                               c2, negm2);
     float x0, x1;
     f2_unpack_f(x, x0, x1);
-#endif
     float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
     if (TAIL) {
       if (e0 >= valid) p0 = 0.f;
