@@ -234,7 +234,7 @@ def fa_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, d
            workspace: torch.Tensor | None = None, stream=None):
     """Gradients (dq, dk, dv) of attention given the forward's o and lse and the output gradient dout.
 
-    q, o, dout [B, H, Nq, d] bf16; k, v [B, Hkv, Nk, d] bf16; lse [B, H, Nq] fp32 from fa_fwd.
+    q, o, dout [B, H, Nq, d]; k, v [B, Hkv, Nk, d], all bf16 or all fp32; lse [B, H, Nq] fp32 from fa_fwd.
     """
     for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("lse", lse)):
         _need_cuda_contig(n, t)

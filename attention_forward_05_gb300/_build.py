@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libfa.so")
 SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp32.cu", "fa_fwd_merge.cu", "fa_decode.cu",
-           "fa_decode_noalloc.cu", "fa_bwd.cu",
+           "fa_decode_noalloc.cu", "fa_bwd.cu", "fa_bwd_fp32.cu",
            "fa_decode_gqa.cu", "fa_fwd_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -516,7 +516,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_BF16) return FA_ERR_UNSUPPORTED;  // fp32 gradients are not built
+  if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
@@ -545,25 +545,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if (own_ws) cudaFreeAsync(ws, st);
     return e != cudaSuccess ? cuda_fail(e) : FA_ERR_CUDA;
   };
-  CUtensorMap kk, vk, qk, dok, qq, doq, kq, vq;
-  if (encode_map(&kk, k, true, BHkv, Nk, d, 64, geo.kv_keys) != FA_OK ||
-      encode_map(&vk, v, true, BHkv, Nk, d, 64, geo.kv_keys) != FA_OK ||
-      encode_map(&qk, q, true, BHi, Nq, d, 64, geo.kv_qrows) != FA_OK ||
-      encode_map(&dok, dout, true, BHi, Nq, d, 64, geo.kv_qrows) != FA_OK ||
-      encode_map(&qq, q, true, BHi, Nq, d, 64, geo.q_rows) != FA_OK ||
-      encode_map(&doq, dout, true, BHi, Nq, d, 64, geo.q_rows) != FA_OK ||
-      encode_map(&kq, k, true, BHkv, Nk, d, 64, geo.q_keys) != FA_OK ||
-      encode_map(&vq, v, true, BHkv, Nk, d, 64, geo.q_keys) != FA_OK)
-    return fail(cudaSuccess);
   fa::BwdLaunch a;
-  a.tm_k_kv = &kk;
-  a.tm_v_kv = &vk;
-  a.tm_q_kv = &qk;
-  a.tm_do_kv = &dok;
-  a.tm_q_q = &qq;
-  a.tm_do_q = &doq;
-  a.tm_k_q = &kq;
-  a.tm_v_q = &vq;
+  a.q = q;
+  a.k = k;
+  a.v = v;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
@@ -571,6 +556,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.dk = dk;
   a.dv = dv;
   a.rowv = reinterpret_cast<float*>(ws);
+  a.rowv2 = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(BHi) * nq_pad * sizeof(float)));
   a.err = err;
   a.BH = BHi;
   a.BHkv = BHkv;
@@ -583,8 +569,34 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.causal = causal;
   a.c = scale * 1.4426950408889634f;
   a.scale = scale;
-  a.fault = g_fault.exchange(0);
+  a.fault = g_fault.exchange(0);  // consumed by either dtype; only the bf16 kernels have waits to fault
   a.stream = st;
+  if (dtype == FA_FP32) {
+    cudaError_t e = nq_pad % fa::bwd_fp32_nq_align() == 0 ? fa::launch_bwd_fp32(a) : cudaErrorInvalidValue;
+    if (own_ws) {
+      cudaError_t e2 = cudaFreeAsync(ws, st);
+      if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? FA_OK : cuda_fail(e);
+  }
+  CUtensorMap kk, vk, qk, dok, qq, doq, kq, vq;
+  if (encode_map(&kk, k, true, BHkv, Nk, d, 64, geo.kv_keys) != FA_OK ||
+      encode_map(&vk, v, true, BHkv, Nk, d, 64, geo.kv_keys) != FA_OK ||
+      encode_map(&qk, q, true, BHi, Nq, d, 64, geo.kv_qrows) != FA_OK ||
+      encode_map(&dok, dout, true, BHi, Nq, d, 64, geo.kv_qrows) != FA_OK ||
+      encode_map(&qq, q, true, BHi, Nq, d, 64, geo.q_rows) != FA_OK ||
+      encode_map(&doq, dout, true, BHi, Nq, d, 64, geo.q_rows) != FA_OK ||
+      encode_map(&kq, k, true, BHkv, Nk, d, 64, geo.q_keys) != FA_OK ||
+      encode_map(&vq, v, true, BHkv, Nk, d, 64, geo.q_keys) != FA_OK)
+    return fail(cudaSuccess);
+  a.tm_k_kv = &kk;
+  a.tm_v_kv = &vk;
+  a.tm_q_kv = &qk;
+  a.tm_do_kv = &dok;
+  a.tm_q_q = &qq;
+  a.tm_do_q = &doq;
+  a.tm_k_q = &kq;
+  a.tm_v_q = &vq;
   cudaError_t e = fa::launch_bwd_bf16(a);
   if (own_ws) {
     cudaError_t e2 = cudaFreeAsync(ws, st);

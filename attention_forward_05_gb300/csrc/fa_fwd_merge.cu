@@ -54,14 +54,37 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_CTA)
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int i = 0; i < n_split; ++i) {
-    const int sp = order == nullptr ? i : (invalid ? 0 : order[i]);
-    const float2 ml = ws_ml[sp * rows + row];
-    const float w = ex2_approx(ml.x - M);
-    L = fmaf(ml.y, w, L);
-    const float* src = ws_o + (sp * rows + row) * D;
+  // Splits in groups of 32: lane i fetches the (m, l) of the group's i-th split in merge order and
+  // forms its weight 2^(m - M); then the states accumulate in merge order, 8 splits' rows loaded at a
+  // time, so that the loads of a group are in flight together rather than one after another.
+  for (int i0 = 0; i0 < n_split; i0 += 32) {
+    const int cnt = min(32, n_split - i0);
+    const int i = i0 + lane;
+    const int sp_l = i < n_split ? (order == nullptr ? i : (invalid ? 0 : order[i])) : 0;
+    const float2 ml_l = i < n_split ? ws_ml[sp_l * rows + row] : make_float2(-INFINITY, 0.f);
+    const float w_l = i < n_split ? ex2_approx(ml_l.x - M) : 0.f;
+    for (int u0 = 0; u0 < cnt; u0 += 8) {
+      float v[8][PER];
+      float w[8], lsp[8];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = fmaf(src[lane + 32 * e], w, acc[e]);
+      for (int u = 0; u < 8; ++u) {
+        const int src_lane = (u0 + u) & 31;
+        const int sp = __shfl_sync(0xffffffffu, sp_l, src_lane);
+        w[u] = __shfl_sync(0xffffffffu, w_l, src_lane);
+        lsp[u] = __shfl_sync(0xffffffffu, ml_l.y, src_lane);
+        const float* src = ws_o + (sp * rows + row) * D;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) v[u][e] = (u0 + u < cnt) ? src[lane + 32 * e] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u0 + u < cnt) {
+          L = fmaf(lsp[u], w[u], L);
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(v[u][e], w[u], acc[e]);
+        }
+      }
+    }
   }
   const float inv = invalid ? __int_as_float(0x7fc00000) : 1.f / L;
 #pragma unroll

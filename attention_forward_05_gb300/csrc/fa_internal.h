@@ -107,13 +107,18 @@ struct BwdLaunch {
   const CUtensorMap* tm_do_q;
   const CUtensorMap* tm_k_q;
   const CUtensorMap* tm_v_q;
-  const void* o;            // [BH, Nq, d] bf16 forward output
-  const void* dout;         // [BH, Nq, d] bf16
+  const void* q;            // [BH, Nq, d] (read directly by the fp32 kernels; bf16 reads through the maps)
+  const void* k;            // [BHkv, Nk, d]
+  const void* v;
+  const void* o;            // [BH, Nq, d] forward output, in the inputs' dtype
+  const void* dout;         // [BH, Nq, d]
   const float* lse;         // [BH, Nq] natural-log LSE of the forward
-  void* dq;                 // [BH, Nq, d] bf16
-  void* dk;                 // [BHkv, Nk, d] bf16
+  void* dq;                 // [BH, Nq, d]
+  void* dk;                 // [BHkv, Nk, d]
   void* dv;
-  float* rowv;              // workspace [BH][Nq_pad/2][4]: (-L log2 e, -D) interleaved by row pairs
+  float* rowv;              // bf16: workspace [BH][Nq_pad/2][4]: (-L log2 e, -D) interleaved by row pairs;
+                            // fp32: [BH][Nq_pad] of -L log2 e
+  float* rowv2;             // fp32: [BH][Nq_pad] of -D
   int* err;
   int BH, BHkv, H, Hkv, Nq, Nk, Nq_pad, d;
   int causal;
@@ -134,6 +139,10 @@ struct BwdGeometry {
 BwdGeometry bwd_geometry(int d);
 // prep pass, then dK/dV, then dQ, in stream order
 cudaError_t launch_bwd_bf16(const BwdLaunch& a);
+// fp32 tensors, fp32 arithmetic on the CUDA cores (fa_bwd_fp32.cu); the same three launches.  Nq_pad
+// must be a multiple of bwd_fp32_nq_align().
+cudaError_t launch_bwd_fp32(const BwdLaunch& a);
+int bwd_fp32_nq_align();
 
 struct DecodeLaunch {
   const void* q;            // [BH, d] bf16

@@ -551,8 +551,9 @@ def measure_extras(fa, torch, accounting, dev, stream, launches=20, hbm_gbs=None
       split_kv      B=1 H=1 N=4096 d=64 fp32 (TF32) with automatic key splits vs one split
       decode_gqa    the decode workload (B=32, H=32 query heads, Nk=32768, d=64, 16 splits) with 8 and 4
                     key/value heads (groups of 4 and 8), GB/s of K/V read once plus q and o
-      bwd           fa_bwd on the two bf16 prefill workloads, plain and causal (FLOPs of the five
-                    backward contractions, 2.5x the forward's)
+      bwd           fa_bwd on the two bf16 prefill workloads, plain and causal, and on the fp32
+                    single-head N=4096 workload (FLOPs of the five backward contractions, 2.5x the
+                    forward's)
     """
     from attention_forward_05_gb300.inputs import WORKLOADS, make_dout, make_qkv, workload_inputs
 
@@ -610,6 +611,17 @@ def measure_extras(fa, torch, accounting, dev, stream, launches=20, hbm_gbs=None
             fl = (accounting.bwd_flops_causal if causal else accounting.bwd_flops)(w.B, w.H, w.Nq, w.Nk, w.d)
             out[f"bwd_{'causal_' if causal else ''}{name}"] = {"ms": ms, "tflops": fl / ms / 1e9}
         del q, k, v, dout, grads, o, lse
+    w = WORKLOADS["long_fp32"]
+    q, k, v = workload_inputs(w, device=dev)
+    dout = make_dout(w.B, w.H, w.Nq, w.d, "fp32", seed=w.seed + 700, device=dev)
+    o, lse = fa.fa_fwd(q, k, v, scale=w.scale, stream=stream)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale, dq=grads[0], dk=grads[1], dv=grads[2],
+                                 workspace=ws, stream=stream))
+    out["bwd_long_fp32"] = {"ms": ms, "tflops": accounting.bwd_flops(w.B, w.H, w.Nq, w.Nk, w.d) / ms / 1e9,
+                            "arithmetic": "fp32 FMA on the CUDA cores"}
+    del q, k, v, dout, grads, o, lse
     if fa.fa_check_device_error() != fa.FA_OK:
         raise RuntimeError("device timeout in the extra measurements")
     return out

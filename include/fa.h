@@ -134,7 +134,7 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d,
                                    int causal);
 
 /*
- * fa_bwd -- gradients of exact attention (bf16 operands, fp32 accumulation).
+ * fa_bwd -- gradients of exact attention (bf16 or fp32 tensors).
  * Given the forward's inputs, its output O and natural-log LSE, and dO (the
  * gradient of a loss with respect to O), writes
  *   dV = P^T dO, dQ = scale dS K, dK = scale dS^T Q, with P = exp(scale Q K^T - LSE)
@@ -142,11 +142,14 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d,
  *   (Level 2-3)", Exercise 5: the forward keeps O and the row statistics, the
  *   backward rebuilds P_ij and accumulates dV_j += P_ij^T dO_i), dP = dO V^T and
  *   dS = P * (dP - D), D_i = sum_c dO_ic O_ic (chain rule through the softmax).
- *   q, o, dout, dq  [B, H, Nq, d] bf16       k, v, dk, dv [B, Hkv, Nk, d] bf16
+ *   q, o, dout, dq  [B, H, Nq, d] in dtype   k, v, dk, dv [B, Hkv, Nk, d] in dtype
  *   lse             [B, H, Nq] fp32 in: as written by fa_fwd / fa_fwd_ex
  *   Hkv, causal     as in fa_fwd_ex; with Hkv < H, dk and dv sum over the query
  *                   heads that share a key/value head.
- *   dtype           FA_BF16 only (FA_FP32 returns FA_ERR_UNSUPPORTED); d 64 or 128.
+ *   dtype           FA_BF16: bf16 operands on the tensor cores, fp32 accumulation,
+ *                   P and dS rounded to bf16 for their products.
+ *                   FA_FP32: every product and sum in fp32 on the CUDA cores (the
+ *                   tensor cores would round the operands to tf32).  d 64 or 128.
  *   workspace       device buffer of at least fa_bwd_workspace_bytes(B, H, Nq, d)
  *                   bytes (16-byte aligned) for D and the rescaled LSE, or NULL
  *                   to allocate it stream-ordered on `stream`.
@@ -274,6 +277,7 @@ const char* fa_last_cuda_error_string(void);
  * copy, or the load warp of the backward's dK/dV kernel skip its key/value
  * copy (and the expected-byte count), so the consumers' bounded waits run
  * out, the kernel abandons its work, records FA_ERR_TIMEOUT and returns.
+ * An fp32 fa_bwd call disarms it without effect (its kernels have no waits).
  * mode 0 disarms.  Returns FA_OK or FA_ERR_INVALID_ARG.
  */
 int fa_debug_set_fault(int mode);

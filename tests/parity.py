@@ -189,12 +189,25 @@ def check_decode(q, k, v, o, lse, scale: float, splits: int, order=None, heads=N
 TOL_BWD = dict(max_rel=4 * 2.0 ** -8, mean_rel=2 * 2.0 ** -8)
 
 
-def check_bwd(q, k, v, dout, dq, dk, dv, scale: float, causal: bool = False, name: str = "") -> dict:
+# fp32 backward (fp32 products and sums on the CUDA cores), fed the oracle's own O and LSE so that
+# only its arithmetic is measured.  With u = 2^-24, one score carries at most d u |scale| sum_c |q_c k_c|
+# of rounding (the dot-product bound), 2e-5 at d = 64 and 5.5e-5 at d = 128 for N(0,1) inputs (about
+# 1e-6 typically, the rounding errors being independent), and ex2.approx adds about 2^-22 relative
+# to P.  Gradients inherit that relative error through P and dS; the bounds leave a margin of about 2
+# over the worst case for the maximum and about 10 over the typical case for the mean.
+TOL_BWD_FP32 = dict(max_rel=1e-4, mean_rel=1e-5)
+# fp32 backward after the library's fp32-in forward: O and LSE then carry the forward's tf32 products
+# (u = 2^-11), which P and D inherit; the bf16 reasoning above with u = 2^-11 gives these bounds.
+TOL_BWD_TF32_FWD = dict(max_rel=4 * 2.0 ** -11, mean_rel=2 * 2.0 ** -11)
+
+
+def check_bwd(q, k, v, dout, dq, dk, dv, scale: float, causal: bool = False, name: str = "", tol=None) -> dict:
     """GPU gradients against the oracle's float64 gradients on the same input bytes.
 
-    For each of dQ, dK, dV: max|err| / max|ref| <= TOL_BWD['max_rel'] and
-    mean|err| / mean|ref| <= TOL_BWD['mean_rel'].
+    For each of dQ, dK, dV: max|err| / max|ref| <= tol['max_rel'] and
+    mean|err| / mean|ref| <= tol['mean_rel'] (tol defaults to TOL_BWD).
     """
+    tol = TOL_BWD if tol is None else tol
     ref = oracle.attention_bwd(q, k, v, dout, scale, causal=causal)
     res = {}
     for nm, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
@@ -206,6 +219,6 @@ def check_bwd(q, k, v, dout, dq, dk, dv, scale: float, causal: bool = False, nam
         res[nm + "_mean_rel"] = float(err.mean() / max(np.abs(r).mean(), 1e-30))
     print(f"[parity] {name}: " + " ".join(f"{k}={v:.3e}" for k, v in res.items()))
     for nm in ("dq", "dk", "dv"):
-        assert res[nm + "_max_rel"] <= TOL_BWD["max_rel"], f"{name}: {nm} max rel err {res[nm + '_max_rel']:.3e}"
-        assert res[nm + "_mean_rel"] <= TOL_BWD["mean_rel"], f"{name}: {nm} mean rel err {res[nm + '_mean_rel']:.3e}"
+        assert res[nm + "_max_rel"] <= tol["max_rel"], f"{name}: {nm} max rel err {res[nm + '_max_rel']:.3e}"
+        assert res[nm + "_mean_rel"] <= tol["mean_rel"], f"{name}: {nm} mean rel err {res[nm + '_mean_rel']:.3e}"
     return res

@@ -193,7 +193,7 @@ def _bwd(**kw):
     (dict(causal=1, Nq=300), fa.FA_ERR_INVALID_ARG),
     (dict(causal=3), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
-    (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), fa.FA_ERR_UNSUPPORTED),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(ws=P, ws_bytes=16), fa.FA_ERR_INVALID_ARG),
     (dict(ws=P + 4, ws_bytes=1 << 20), fa.FA_ERR_INVALID_ARG),

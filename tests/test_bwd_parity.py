@@ -12,8 +12,8 @@ import torch
 
 import attention_forward_05_gb300 as fa
 import oracle
-from attention_forward_05_gb300.inputs import make_dout, make_qkv
-from parity import TOL_BWD, check_bwd
+from attention_forward_05_gb300.inputs import WORKLOADS, make_dout, make_qkv, workload_inputs
+from parity import TOL_BWD, TOL_BWD_FP32, TOL_BWD_TF32_FWD, check_bwd
 
 pytestmark = pytest.mark.gpu
 
@@ -105,12 +105,72 @@ def test_bwd_deterministic_and_caller_workspace(cuda_device):
         fa.fa_bwd(q, k, v, o, dout, lse, workspace=ws[: nbytes - 256])
 
 
-def test_bwd_rejects_fp32(cuda_device):
-    q, k, v = make_qkv(1, 1, 64, 64, 64, "fp32", seed=1600, device=cuda_device)
-    o, lse = fa.fa_fwd(q, k, v)
-    with pytest.raises(fa.FAError) as ei:
-        fa.fa_bwd(q, k, v, o, o.clone(), lse)
-    assert ei.value.status == fa.FA_ERR_UNSUPPORTED
+# ----------------------------------------------------------------- fp32 tensors
+# The pages' backward exercise is written for fp32 tensors ("Flash Attention 代码填空 (Level 2-3)",
+# Exercise 5).  These cases give the fp32 backward the oracle's own O and LSE (rounded to fp32), so
+# that its arithmetic alone is compared with the oracle's gradients at fp32 tolerances.
+
+def _run_fp32_oracle_stats(q, k, v, dout, causal=False, scale=None):
+    d = q.shape[-1]
+    sc = 1 / math.sqrt(d) if scale is None else scale
+    ref_o, ref_lse = oracle.attention(q, k, v, sc, causal=causal)
+    o = torch.from_numpy(ref_o).float().to(q.device)
+    lse = torch.from_numpy(ref_lse).float().to(q.device)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, dout, lse, scale=sc, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    return sc, dq, dk, dv
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bwd_fp32_shapes(cuda_device, d, shape):
+    B, H, Nq, Nk = shape
+    q, _, _ = make_qkv(B, H, Nq, 1, d, "fp32", seed=1800 + Nq + d, device=cuda_device)
+    _, k, v = make_qkv(B, H, 1, Nk, d, "fp32", seed=1801 + Nk + d, device=cuda_device)
+    dout = make_dout(B, H, Nq, d, "fp32", seed=1802 + Nq, device=cuda_device)
+    sc, dq, dk, dv = _run_fp32_oracle_stats(q, k, v, dout)
+    assert dq.dtype == torch.float32
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, name=f"bwd fp32 d{d} {shape}", tol=TOL_BWD_FP32)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_fp32_causal_and_grouped_heads(cuda_device, d, causal):
+    B, H, Hkv, Nq, Nk = 2, 4, 2, 300, 400
+    q, _, _ = make_qkv(B, H, Nq, 1, d, "fp32", seed=1900 + d, device=cuda_device)
+    _, k, v = make_qkv(B, Hkv, 1, Nk, d, "fp32", seed=1901 + d, device=cuda_device)
+    dout = make_dout(B, H, Nq, d, "fp32", seed=1902, device=cuda_device)
+    sc, dq, dk, dv = _run_fp32_oracle_stats(q, k, v, dout, causal=causal)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, causal=causal, name=f"bwd fp32 gqa d{d} causal={causal}",
+              tol=TOL_BWD_FP32)
+
+
+def test_bwd_fp32_peaked_and_scale_one(cuda_device):
+    q, k, v = make_qkv(1, 2, 256, 384, 64, "fp32", seed=1950, qk_mult=3.0, device=cuda_device)
+    dout = make_dout(1, 2, 256, 64, "fp32", seed=1951, device=cuda_device)
+    sc, dq, dk, dv = _run_fp32_oracle_stats(q, k, v, dout)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, name="bwd fp32 peaked", tol=TOL_BWD_FP32)
+    q, k, v = make_qkv(1, 1, 130, 70, 64, "fp32", seed=1952, qk_mult=0.3, device=cuda_device)
+    dout = make_dout(1, 1, 130, 64, "fp32", seed=1953, device=cuda_device)
+    sc, dq, dk, dv = _run_fp32_oracle_stats(q, k, v, dout, scale=1.0)
+    check_bwd(q, k, v, dout, dq, dk, dv, sc, name="bwd fp32 scale=1", tol=TOL_BWD_FP32)
+
+
+def test_bwd_fp32_after_library_forward_and_deterministic(cuda_device):
+    """The training-step pipeline on fp32 tensors: fa_fwd (tf32 products) then fa_bwd; the gradients
+    carry the forward's tf32 rounding through O and LSE.  Repeated calls are bit-identical."""
+    w = WORKLOADS["long_fp32"]
+    q, k, v = workload_inputs(w, device=cuda_device)
+    dout = make_dout(w.B, w.H, w.Nq, w.d, "fp32", seed=1960, device=cuda_device)
+    o, lse = fa.fa_fwd(q, k, v, scale=w.scale)
+    a = fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale)
+    b = fa.fa_bwd(q, k, v, o, dout, lse, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    check_bwd(q, k, v, dout, *a, w.scale, name="bwd fp32 after fwd, N=4096", tol=TOL_BWD_TF32_FWD)
 
 
 def test_bwd_full_size_d64(cuda_device):
