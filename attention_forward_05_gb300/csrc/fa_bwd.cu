@@ -9,45 +9,18 @@ namespace fa {
 
 // Tile choices.  dK/dV: 128 keys per CTA, 64 query rows per step; the ring of Q/dO tiles is deep
 // enough that copies land before the MMA warp reaches them (it only refills a stage after the
-// gradient MMAs of the step it held have completed).
+// gradient MMAs of the step it held have completed): 8 stages at d = 64, 4 at d = 128.
 // dQ: two 128-row query tiles per CTA, 64 keys per step; K/V rings of 6 stages at d = 64 (+0.8% over 4)
-// and 3 at d = 128 (+1.7% over 2).  The FA_BWD_*_STAGES definitions override them in tuning builds.
+// and 3 at d = 128 (+1.7% over 2).
 // d=64 uses three score slots in TMEM (512 columns), d=128 two (its dV and dK take 256).
-// HALF: the gradient (dV, dK) or dQ MMAs of a step start once the first half of its columns is
-// written (d = 128: +4.6%); the FA_BWD_* macros override the choice in tuning builds.
-#ifndef FA_BWD_KV64_HALF
-#define FA_BWD_KV64_HALF 0
-#endif
-#ifndef FA_BWD_Q64_HALF
-#define FA_BWD_Q64_HALF 0
-#endif
-#ifndef FA_BWD_KV128_HALF
-#define FA_BWD_KV128_HALF 1
-#endif
-#ifndef FA_BWD_Q128_HALF
-#define FA_BWD_Q128_HALF 1
-#endif
+// HALF (d = 128 only): the gradient (dV, dK) or dQ MMAs of a step start once the first half of its
+// columns is written (+4.6%; 1-2% slower at d = 64).
 // ATMEM (d = 64 only: tensor memory has no room at d = 128): the dQ kernel's S and dP MMAs take Q and
 // dO from tensor memory.
-#ifndef FA_BWD_Q64_ATMEM
-#define FA_BWD_Q64_ATMEM 1
-#endif
-#ifndef FA_BWD_KV128_STAGES
-#define FA_BWD_KV128_STAGES 4
-#endif
-#ifndef FA_BWD_Q128_STAGES
-#define FA_BWD_Q128_STAGES 3
-#endif
-#ifndef FA_BWD_KV64_STAGES
-#define FA_BWD_KV64_STAGES 8
-#endif
-#ifndef FA_BWD_Q64_STAGES
-#define FA_BWD_Q64_STAGES 6
-#endif
-using BwdKV64 = BwdKVCfg<64, 64, FA_BWD_KV64_STAGES, 3, FA_BWD_KV64_HALF != 0>;
-using BwdKV128 = BwdKVCfg<128, 64, FA_BWD_KV128_STAGES, 2, FA_BWD_KV128_HALF != 0>;
-using BwdQ64 = BwdQCfg<64, 64, FA_BWD_Q64_STAGES, FA_BWD_Q64_HALF != 0, FA_BWD_Q64_ATMEM != 0>;
-using BwdQ128 = BwdQCfg<128, 64, FA_BWD_Q128_STAGES, FA_BWD_Q128_HALF != 0>;
+using BwdKV64 = BwdKVCfg<64, 64, 8, 3, false>;
+using BwdKV128 = BwdKVCfg<128, 64, 4, 2, true>;
+using BwdQ64 = BwdQCfg<64, 64, 6, false, true>;
+using BwdQ128 = BwdQCfg<128, 64, 3, true>;
 
 // D_i = sum_c dO_ic O_ic (fp32 over the bf16 inputs) and nl_i = -L_i log2(e) for the rows of
 // [BH][Nq_pad], written interleaved by row pairs: rowv[pair] = (nl_2i, nl_2i+1, -D_2i, -D_2i+1)

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_fp32_kernel(const float* __re
                                                                const float* __restrict__ lse, float* __restrict__ nl,
                                                                float* __restrict__ negd, long long rows_pad, int Nq,
                                                                int Nq_pad) {
+  griddep_launch_dependents();  // the dK/dV kernel may start its set-up; it waits for this grid's rows
   constexpr int LPR = D / 4;  // lanes per row, one float4 each (a row is D / 4 lanes of one warp)
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long r = gt / LPR;
@@ -127,6 +128,11 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF
   const float* vg = p.v + (static_cast<size_t>(bhkv) * p.Nk + k0) * D;
   load_transposed<D>(kt, PAD_M, kg, BW_M, kvalid);
   load_transposed<D>(vt, PAD_M, vg, BW_M, kvalid);
+  // The prep grid's row values are read below, after its completion.  Once every CTA of this grid has
+  // passed that point the dQ grid, which reads the same values and nothing this grid writes, may start
+  // on the SMs this grid leaves idle.
+  griddep_wait();
+  griddep_launch_dependents();
 
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   // score tile: keys 4 ty .. 4 ty + 3, query rows 2 tx, 2 tx + 1 of the step
@@ -345,6 +351,9 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32
 #pragma unroll
     for (int c = 0; c < CW; ++c) p.dq[off + c] = dq_acc[r][c] * p.scale;
   }
+  // This grid may have started before the dK/dV grid finished; waiting for it here keeps every gradient
+  // complete once this grid is, for the work that follows the backward on the stream.
+  griddep_wait();
 }
 
 template <int D>
@@ -368,10 +377,11 @@ cudaError_t launch_bwd_fp32_d(const BwdLaunch& a, const BwdF32Params& p) {
   const long long grid_kv = static_cast<long long>((a.Nk + BW_M - 1) / BW_M) * a.BHkv;
   const long long grid_q = static_cast<long long>((a.Nq + BW_M - 1) / BW_M) * a.BH;
   if (grid_kv <= 0 || grid_kv > 0x7FFFFFFFLL || grid_q <= 0 || grid_q > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  fa_bwd_dkdv_fp32_kernel<D><<<static_cast<unsigned>(grid_kv), BW_THREADS, smem_kv, a.stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  fa_bwd_dq_fp32_kernel<D><<<static_cast<unsigned>(grid_q), BW_THREADS, smem_q, a.stream>>>(p);
-  return cudaGetLastError();
+  // prep -> dK/dV -> dQ as programmatic dependents (see the kernels for what each waits for)
+  if ((e = launch_dependent(fa_bwd_dkdv_fp32_kernel<D>, static_cast<unsigned>(grid_kv), BW_THREADS, smem_kv,
+                            a.stream, p)) != cudaSuccess)
+    return e;
+  return launch_dependent(fa_bwd_dq_fp32_kernel<D>, static_cast<unsigned>(grid_q), BW_THREADS, smem_q, a.stream, p);
 }
 
 }  // namespace

@@ -32,7 +32,7 @@ def main(argv=None) -> int:
     ap.add_argument("--H", type=int, default=0)
     ap.add_argument("--time", action="store_true", help="time the launches with CUDA events and print the rate")
     ap.add_argument("--causal", action="store_true", help="causal mask (prefill workloads)")
-    ap.add_argument("--bwd", action="store_true", help="time the backward (fa_bwd) after one forward (bf16 prefill)")
+    ap.add_argument("--bwd", action="store_true", help="time the backward (fa_bwd) after one forward (prefill)")
     ap.add_argument("--hkv", type=int, default=0, help="decode: grouped-query decode with this many key/value heads")
     a = ap.parse_args(argv)
     w = WORKLOADS[a.workload]
@@ -51,9 +51,9 @@ def main(argv=None) -> int:
     lse = torch.empty((w.B, w.H, w.Nq), device=dev) if not w.splits else None
 
     if a.bwd:
-        if w.splits or w.dtype != "bf16":
-            ap.error("--bwd takes a bf16 prefill workload")
-        dout = make_dout(w.B, w.H, w.Nq, w.d, "bf16", seed=w.seed + 700, device=dev)
+        if w.splits:
+            ap.error("--bwd takes a prefill workload")
+        dout = make_dout(w.B, w.H, w.Nq, w.d, w.dtype, seed=w.seed + 700, device=dev)
         fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse, causal=a.causal)
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
         ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq, w.d), dtype=torch.uint8, device=dev)
