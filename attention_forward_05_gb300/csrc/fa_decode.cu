@@ -212,13 +212,38 @@ __global__ void __launch_bounds__(MERGE_THREADS) fa_decode_merge_kernel(
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int i = 0; i < splits; ++i) {
-    const int cidx = (order == nullptr) ? i : (invalid ? 0 : order[i]);
-    const float mc = mh[cidx];
-    const float w = (mc == -INFINITY) ? 0.f : ex2_approx(mc - M);
-    Ls = fmaf(lh[cidx], w, Ls);
+  // Chunks in groups of 32: lane i fetches the (m, l) of the group's i-th chunk in merge order and
+  // forms its weight; the states then accumulate in merge order, eight chunks' o rows loaded at a time
+  // so that a head's loads are in flight together rather than one after another.
+  for (int i0 = 0; i0 < splits; i0 += 32) {
+    const int cnt = min(32, splits - i0);
+    const int i = i0 + lane;
+    const int c_l = i < splits ? ((order == nullptr) ? i : (invalid ? 0 : order[i])) : 0;
+    const float m_l = i < splits ? mh[c_l] : -INFINITY;
+    const float l_l = i < splits ? lh[c_l] : 0.f;
+    const float w_l = (m_l == -INFINITY) ? 0.f : ex2_approx(m_l - M);
+    for (int u0 = 0; u0 < cnt; u0 += 8) {
+      float v[8][PER];
+      float w[8], lw[8];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = fmaf(oh[static_cast<size_t>(cidx) * D + lane + 32 * e], w, acc[e]);
+      for (int u = 0; u < 8; ++u) {
+        const int src_lane = (u0 + u) & 31;
+        const int cidx = __shfl_sync(0xffffffffu, c_l, src_lane);
+        w[u] = __shfl_sync(0xffffffffu, w_l, src_lane);
+        lw[u] = __shfl_sync(0xffffffffu, l_l, src_lane);
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          v[u][e] = (u0 + u < cnt) ? oh[static_cast<size_t>(cidx) * D + lane + 32 * e] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u0 + u < cnt) {
+          Ls = fmaf(lw[u], w[u], Ls);
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(v[u][e], w[u], acc[e]);
+        }
+      }
+    }
   }
   const float inv = invalid ? __int_as_float(0x7fc00000) : 1.f / Ls;
 #pragma unroll
