@@ -68,24 +68,44 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_fp32_kernel(const float* __re
   }
 }
 
-// dst[c][r] = src[r][c] for rows r < nrows of a [*, D] fp32 block (rows >= valid read as zero);
-// dst has `ld` words per c.
-template <int D>
-__device__ __forceinline__ void load_transposed(float* dst, int ld, const float* src, int nrows, int valid) {
-  for (int idx = threadIdx.x; idx < nrows * D; idx += BW_THREADS) {
+// dst[c][r] = src[r][c] for the NROWS rows of a [*, D] fp32 block (rows >= valid read as zero); dst
+// has `ld` words per c.  Each thread loads all its elements before storing any, so the block's global
+// loads are in flight together.
+template <int D, int NROWS>
+__device__ __forceinline__ void load_transposed(float* dst, int ld, const float* src, int valid) {
+  constexpr int PER = NROWS * D / BW_THREADS;
+  static_assert(PER * BW_THREADS == NROWS * D, "whole rounds");
+  float x[PER];
+#pragma unroll
+  for (int it = 0; it < PER; ++it) {
+    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
     const int r = idx / D, c = idx % D;
-    dst[c * ld + r] = r < valid ? src[static_cast<size_t>(r) * D + c] : 0.f;
+    x[it] = r < valid ? src[static_cast<size_t>(r) * D + c] : 0.f;
+  }
+#pragma unroll
+  for (int it = 0; it < PER; ++it) {
+    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
+    dst[(idx % D) * ld + idx / D] = x[it];
   }
 }
 
-// dst[r][c] = src[r][c] (row-major, D words per row) for rows r < nrows (rows >= valid read as zero).
-template <int D>
-__device__ __forceinline__ void load_rows(float* dst, const float* src, int nrows, int valid) {
-  for (int idx = threadIdx.x; idx < nrows * D / 4; idx += BW_THREADS) {
+// dst[r][c] = src[r][c] (row-major, D words per row) for the NROWS rows (rows >= valid read as zero).
+template <int D, int NROWS>
+__device__ __forceinline__ void load_rows(float* dst, const float* src, int valid) {
+  constexpr int PER = NROWS * D / 4 / BW_THREADS;
+  static_assert(PER * BW_THREADS * 4 == NROWS * D, "whole rounds");
+  float4 x[PER];
+#pragma unroll
+  for (int it = 0; it < PER; ++it) {
+    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
     const int r = idx / (D / 4), c4 = idx % (D / 4);
-    const float4 x = r < valid ? reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * D)[c4]
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-    reinterpret_cast<float4*>(dst + r * D)[c4] = x;
+    x[it] = r < valid ? reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * D)[c4]
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int it = 0; it < PER; ++it) {
+    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
+    reinterpret_cast<float4*>(dst + (idx / (D / 4)) * D)[idx % (D / 4)] = x[it];
   }
 }
 
@@ -126,8 +146,8 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF
   const int kvalid = min(BW_M, p.Nk - k0);
   const float* kg = p.k + (static_cast<size_t>(bhkv) * p.Nk + k0) * D;
   const float* vg = p.v + (static_cast<size_t>(bhkv) * p.Nk + k0) * D;
-  load_transposed<D>(kt, PAD_M, kg, BW_M, kvalid);
-  load_transposed<D>(vt, PAD_M, vg, BW_M, kvalid);
+  load_transposed<D, BW_M>(kt, PAD_M, kg, kvalid);
+  load_transposed<D, BW_M>(vt, PAD_M, vg, kvalid);
   // The prep grid's row values are read below, after its completion.  Once every CTA of this grid has
   // passed that point the dQ grid, which reads the same values and nothing this grid writes, may start
   // on the SMs this grid leaves idle.
@@ -154,10 +174,10 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF
       __syncthreads();  // the previous step's tiles are no longer read
       const float* qg = p.q + (bh * p.Nq + i0) * D;
       const float* dg = p.dout + (bh * p.Nq + i0) * D;
-      load_transposed<D>(qt, PAD_N, qg, BW_N, qvalid);
-      load_transposed<D>(dot, PAD_N, dg, BW_N, qvalid);
-      load_rows<D>(qr, qg, BW_N, qvalid);
-      load_rows<D>(dor, dg, BW_N, qvalid);
+      load_transposed<D, BW_N>(qt, PAD_N, qg, qvalid);
+      load_transposed<D, BW_N>(dot, PAD_N, dg, qvalid);
+      load_rows<D, BW_N>(qr, qg, qvalid);
+      load_rows<D, BW_N>(dor, dg, qvalid);
       if (threadIdx.x < BW_N) {
         const size_t rr = bh * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= every i0 + BW_N read here
         nl_s[threadIdx.x] = p.nl[rr];
@@ -266,8 +286,8 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32
   const int qvalid = min(BW_M, p.Nq - i0);
   const float* qg = p.q + (static_cast<size_t>(bh) * p.Nq + i0) * D;
   const float* dg = p.dout + (static_cast<size_t>(bh) * p.Nq + i0) * D;
-  load_transposed<D>(qt, PAD_M, qg, BW_M, qvalid);
-  load_transposed<D>(dot, PAD_M, dg, BW_M, qvalid);
+  load_transposed<D, BW_M>(qt, PAD_M, qg, qvalid);
+  load_transposed<D, BW_M>(dot, PAD_M, dg, qvalid);
   if (threadIdx.x < BW_M) {
     const size_t rr = static_cast<size_t>(bh) * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= i0 + BW_M
     nl_s[threadIdx.x] = p.nl[rr];
@@ -291,9 +311,9 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32
     __syncthreads();  // the previous step's tiles are no longer read (and the CTA's tiles are in)
     const float* kg = p.k + (static_cast<size_t>(bhkv) * p.Nk + j0) * D;
     const float* vg = p.v + (static_cast<size_t>(bhkv) * p.Nk + j0) * D;
-    load_transposed<D>(kt, PAD_N, kg, BW_N, kvalid);
-    load_transposed<D>(vt, PAD_N, vg, BW_N, kvalid);
-    load_rows<D>(kr, kg, BW_N, kvalid);
+    load_transposed<D, BW_N>(kt, PAD_N, kg, kvalid);
+    load_transposed<D, BW_N>(vt, PAD_N, vg, kvalid);
+    load_rows<D, BW_N>(kr, kg, kvalid);
     __syncthreads();
     // S = Q K^T and dP = dO V^T for this thread's 4 x 2 block
     float s[4][2], dp[4][2];
