@@ -15,14 +15,14 @@
 // Three launches, no atomics (every gradient element is written by one thread of one CTA):
 //   fa_bwd_prep_fp32_kernel  nl_i = -L_i log2(e) and D_i for every query row (padded rows: -inf, 0)
 //   fa_bwd_dkdv_fp32_kernel  one CTA per (key/value head, 64 keys): walks the query rows of every
-//                            query head sharing the key/value head, 32 at a time, and accumulates
-//                            dV and dK of its keys in registers
-//   fa_bwd_dq_fp32_kernel    one CTA per (query head, 64 query rows): walks the keys 32 at a time and
-//                            accumulates dQ of its rows in registers
-// Both main kernels are shared-memory tiled products: each of the 256 threads owns a 4 x 2 block of
-// the step's 64 x 32 score tile and a 4 x (D/16) block of the accumulated gradient tile.  Operands
-// read along the reduction index are kept transposed in shared memory (one padded row per element
-// of the reduction), so that a warp reads consecutive words.
+//                            query head sharing the key/value head, 64 (d = 64) or 32 (d = 128) at a
+//                            time, and accumulates dV and dK of its keys in registers
+//   fa_bwd_dq_fp32_kernel    one CTA per (query head, 64 query rows): walks the keys 64 or 32 at a time
+//                            and accumulates dQ of its rows in registers
+// Both main kernels are shared-memory tiled products: each of the 256 threads owns a 4 x 4 (d = 64)
+// or 4 x 2 (d = 128) block of the step's score tile and a 4 x (d/16) block of the accumulated
+// gradient tile.  Operands read along the reduction index are kept transposed in shared memory, with
+// rows padded to whole 16-byte groups, so that each thread reads its operands as vectors.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -32,9 +32,6 @@ namespace {
 
 constexpr int BW_THREADS = 256;
 constexpr int BW_M = 64;  // rows owned by a CTA: keys (dK/dV kernel) or query rows (dQ kernel)
-constexpr int BW_N = 32;  // rows streamed per step: query rows (dK/dV) or keys (dQ)
-constexpr int PAD_M = BW_M + 1;
-constexpr int PAD_N = BW_N + 1;
 
 // Row values for the fp32 backward: nl[r] = -L_r log2(e), negd[r] = -D_r over [BH][Nq_pad].
 template <int D>
@@ -116,38 +113,73 @@ struct BwdF32Params {
   float c, scale;
 };
 
-// Shared memory of the dK/dV kernel (floats): K^T, V^T [D][65]; per step Q^T, dO^T [D][33], Q, dO
-// [32][D]; P^T and dS^T as [32 query rows][65]; the step's nl and -D.
+// Tile shapes.  A CTA owns BM = 64 rows (keys in the dK/dV kernel, query rows in the dQ kernel) and
+// streams BN rows of the other side per step: 64 at d = 64, 32 at d = 128 (shared memory).  Thread
+// (ty, tx) of 16 x 16 owns rows 4 ty .. 4 ty + 3 of the CTA's side, and in the step's score tile the
+// TQ = BN / 16 columns TQ tx ..; in the accumulated gradient tile the CW = d / 16 columns CW tx ...
+// Arrays read along the reduction index are transposed, with rows padded to a multiple of 4 floats
+// so that every read is one 16-byte (or 8-byte) load.
+template <int D>
+struct F32Tile {
+  static constexpr int BM = BW_M;
+  static constexpr int BN = D == 64 ? 64 : 32;
+  static constexpr int TQ = BN / 16;
+  static constexpr int CW = D / 16;
+  static constexpr int MP = BM + 4;  // padded row of a transposed BM-row block
+  static constexpr int NP = BN + 4;  // padded row of a transposed BN-row block
+};
+
+template <int N>
+__device__ __forceinline__ void lds_vec(float (&r)[N], const float* p) {
+  static_assert(N == 2 || N == 4, "vector width");
+  if constexpr (N == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    r[0] = x.x;
+    r[1] = x.y;
+    r[2] = x.z;
+    r[3] = x.w;
+  } else {
+    const float2 x = *reinterpret_cast<const float2*>(p);
+    r[0] = x.x;
+    r[1] = x.y;
+  }
+}
+
+// Shared memory of the dK/dV kernel (floats): K^T, V^T [D][MP]; per step Q^T, dO^T [D][NP], Q, dO
+// [BN][D]; P^T and dS^T as [BN query rows][MP]; the step's nl and -D.
 template <int D>
 constexpr int dkdv_smem_floats() {
-  return 2 * D * PAD_M + 2 * D * PAD_N + 2 * BW_N * D + 2 * BW_N * PAD_M + 2 * BW_N;
+  using T = F32Tile<D>;
+  return 2 * D * T::MP + 2 * D * T::NP + 2 * T::BN * D + 2 * T::BN * T::MP + 2 * T::BN;
 }
 
 template <int D>
 __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF32Params p) {
-  extern __shared__ float sm[];
-  float* kt = sm;                       // [D][PAD_M]
-  float* vt = kt + D * PAD_M;           // [D][PAD_M]
-  float* qt = vt + D * PAD_M;           // [D][PAD_N]
-  float* dot = qt + D * PAD_N;          // [D][PAD_N]
-  float* qr = dot + D * PAD_N;          // [BW_N][D]
-  float* dor = qr + BW_N * D;           // [BW_N][D]
-  float* ps = dor + BW_N * D;           // [BW_N][PAD_M]: P^T of the step, by query row
-  float* dss = ps + BW_N * PAD_M;       // [BW_N][PAD_M]: dS^T of the step
-  float* nl_s = dss + BW_N * PAD_M;     // [BW_N]
-  float* nd_s = nl_s + BW_N;            // [BW_N]
+  using T = F32Tile<D>;
+  constexpr int BM = T::BM, BN = T::BN, TQ = T::TQ, CW = T::CW, MP = T::MP, NP = T::NP;
+  extern __shared__ __align__(16) float sm[];
+  float* kt = sm;                       // [D][MP]
+  float* vt = kt + D * MP;              // [D][MP]
+  float* qt = vt + D * MP;              // [D][NP]
+  float* dot = qt + D * NP;             // [D][NP]
+  float* qr = dot + D * NP;             // [BN][D]
+  float* dor = qr + BN * D;             // [BN][D]
+  float* ps = dor + BN * D;             // [BN][MP]: P^T of the step, by query row
+  float* dss = ps + BN * MP;            // [BN][MP]: dS^T of the step
+  float* nl_s = dss + BN * MP;          // [BN]
+  float* nd_s = nl_s + BN;              // [BN]
 
-  const int n_kblk = (p.Nk + BW_M - 1) / BW_M;
+  const int n_kblk = (p.Nk + BM - 1) / BM;
   const int kb = static_cast<int>(blockIdx.x % n_kblk);
   const int bhkv = static_cast<int>(blockIdx.x / n_kblk);
   const int b = bhkv / p.Hkv, hkv = bhkv % p.Hkv;
   const int G = p.H / p.Hkv;
-  const int k0 = kb * BW_M;
-  const int kvalid = min(BW_M, p.Nk - k0);
+  const int k0 = kb * BM;
+  const int kvalid = min(BM, p.Nk - k0);
   const float* kg = p.k + (static_cast<size_t>(bhkv) * p.Nk + k0) * D;
   const float* vg = p.v + (static_cast<size_t>(bhkv) * p.Nk + k0) * D;
-  load_transposed<D, BW_M>(kt, PAD_M, kg, kvalid);
-  load_transposed<D, BW_M>(vt, PAD_M, vg, kvalid);
+  load_transposed<D, BM>(kt, MP, kg, kvalid);
+  load_transposed<D, BM>(vt, MP, vg, kvalid);
   // The prep grid's row values are read below, after its completion.  Once every CTA of this grid has
   // passed that point the dQ grid, which reads the same values and nothing this grid writes, may start
   // on the SMs this grid leaves idle.
@@ -155,9 +187,6 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF
   griddep_launch_dependents();
 
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  // score tile: keys 4 ty .. 4 ty + 3, query rows 2 tx, 2 tx + 1 of the step
-  // gradient tile: keys 4 ty .. 4 ty + 3, columns tx * CW .. tx * CW + CW - 1
-  constexpr int CW = D / 16;
   float dv_acc[4][CW], dk_acc[4][CW];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
@@ -166,74 +195,78 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF
 
   // query rows that see any key of this block: i >= k0 - causal_off under the mask
   const int i_first = p.causal ? max(0, k0 - p.causal_off) : 0;
-  const int i_start = i_first / BW_N * BW_N;
+  const int i_start = i_first / BN * BN;
   for (int g = 0; g < G; ++g) {
     const size_t bh = static_cast<size_t>(b) * p.H + hkv * G + g;
-    for (int i0 = i_start; i0 < p.Nq; i0 += BW_N) {
-      const int qvalid = min(BW_N, p.Nq - i0);
+    for (int i0 = i_start; i0 < p.Nq; i0 += BN) {
+      const int qvalid = min(BN, p.Nq - i0);
       __syncthreads();  // the previous step's tiles are no longer read
       const float* qg = p.q + (bh * p.Nq + i0) * D;
       const float* dg = p.dout + (bh * p.Nq + i0) * D;
-      load_transposed<D, BW_N>(qt, PAD_N, qg, qvalid);
-      load_transposed<D, BW_N>(dot, PAD_N, dg, qvalid);
-      load_rows<D, BW_N>(qr, qg, qvalid);
-      load_rows<D, BW_N>(dor, dg, qvalid);
-      if (threadIdx.x < BW_N) {
-        const size_t rr = bh * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= every i0 + BW_N read here
+      load_transposed<D, BN>(qt, NP, qg, qvalid);
+      load_transposed<D, BN>(dot, NP, dg, qvalid);
+      load_rows<D, BN>(qr, qg, qvalid);
+      load_rows<D, BN>(dor, dg, qvalid);
+      if (threadIdx.x < BN) {
+        const size_t rr = bh * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= every i0 + BN read here
         nl_s[threadIdx.x] = p.nl[rr];
         nd_s[threadIdx.x] = p.negd[rr];
       }
       __syncthreads();
-      // S^T = K Q^T and dP^T = V dO^T for this thread's 4 x 2 block
-      float s[4][2], dp[4][2];
+      // S^T = K Q^T and dP^T = V dO^T for this thread's 4 x TQ block
+      float s[4][TQ], dp[4][TQ];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) s[r][0] = s[r][1] = dp[r][0] = dp[r][1] = 0.f;
-#pragma unroll 8
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int qq = 0; qq < TQ; ++qq) s[r][qq] = dp[r][qq] = 0.f;
+#pragma unroll 4
       for (int c = 0; c < D; ++c) {
-        float a[4], av[4];
+        float a[4], av[4], bq[TQ], bg[TQ];
+        lds_vec(a, kt + c * MP + 4 * ty);
+        lds_vec(av, vt + c * MP + 4 * ty);
+        lds_vec(bq, qt + c * NP + TQ * tx);
+        lds_vec(bg, dot + c * NP + TQ * tx);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          a[r] = kt[c * PAD_M + 4 * ty + r];
-          av[r] = vt[c * PAD_M + 4 * ty + r];
-        }
-        const float b0 = qt[c * PAD_N + 2 * tx], b1 = qt[c * PAD_N + 2 * tx + 1];
-        const float g0 = dot[c * PAD_N + 2 * tx], g1 = dot[c * PAD_N + 2 * tx + 1];
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          s[r][0] = fmaf(a[r], b0, s[r][0]);
-          s[r][1] = fmaf(a[r], b1, s[r][1]);
-          dp[r][0] = fmaf(av[r], g0, dp[r][0]);
-          dp[r][1] = fmaf(av[r], g1, dp[r][1]);
-        }
+          for (int qq = 0; qq < TQ; ++qq) {
+            s[r][qq] = fmaf(a[r], bq[qq], s[r][qq]);
+            dp[r][qq] = fmaf(av[r], bg[qq], dp[r][qq]);
+          }
       }
       // P^T and dS^T; masked pairs (key past Nk or past the row's causal limit, row past Nq) give 0
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const int il = 2 * tx + qq, i = i0 + il;
+      for (int qq = 0; qq < TQ; ++qq) {
+        const int il = TQ * tx + qq, i = i0 + il;
         const float nli = nl_s[il], ndi = nd_s[il];
+        float pr[4], dsr[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int kl = 4 * ty + r, kj = k0 + kl;
+          const int kj = k0 + 4 * ty + r;
           const bool vis = kj < p.Nk && i < p.Nq && (!p.causal || kj <= i + p.causal_off);
-          const float pr = vis ? ex2_approx(fmaf(s[r][qq], p.c, nli)) : 0.f;
-          ps[il * PAD_M + kl] = pr;
-          dss[il * PAD_M + kl] = pr * (dp[r][qq] + ndi);
+          pr[r] = vis ? ex2_approx(fmaf(s[r][qq], p.c, nli)) : 0.f;
+          dsr[r] = pr[r] * (dp[r][qq] + ndi);
         }
+        *reinterpret_cast<float4*>(ps + il * MP + 4 * ty) = make_float4(pr[0], pr[1], pr[2], pr[3]);
+        *reinterpret_cast<float4*>(dss + il * MP + 4 * ty) = make_float4(dsr[0], dsr[1], dsr[2], dsr[3]);
       }
       __syncthreads();
       // dV += P^T dO, dK += dS^T Q over the step's query rows
 #pragma unroll 4
-      for (int il = 0; il < BW_N; ++il) {
+      for (int il = 0; il < BN; ++il) {
         float pr[4], dr[4], go[CW], qv[CW];
+        lds_vec(pr, ps + il * MP + 4 * ty);
+        lds_vec(dr, dss + il * MP + 4 * ty);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          pr[r] = ps[il * PAD_M + 4 * ty + r];
-          dr[r] = dss[il * PAD_M + 4 * ty + r];
-        }
+        for (int c4 = 0; c4 < CW; c4 += 4) {
+          float t0[4], t1[4];
+          lds_vec(t0, dor + il * D + tx * CW + c4);
+          lds_vec(t1, qr + il * D + tx * CW + c4);
 #pragma unroll
-        for (int c = 0; c < CW; ++c) {
-          go[c] = dor[il * D + tx * CW + c];
-          qv[c] = qr[il * D + tx * CW + c];
+          for (int e = 0; e < 4; ++e) {
+            go[c4 + e] = t0[e];
+            qv[c4 + e] = t1[e];
+          }
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -251,112 +284,120 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF
     if (kl >= kvalid) continue;
     const size_t off = (static_cast<size_t>(bhkv) * p.Nk + k0 + kl) * D + tx * CW;
 #pragma unroll
-    for (int c = 0; c < CW; ++c) {
-      p.dv[off + c] = dv_acc[r][c];
-      p.dk[off + c] = dk_acc[r][c] * p.scale;
+    for (int c4 = 0; c4 < CW; c4 += 4) {
+      *reinterpret_cast<float4*>(p.dv + off + c4) =
+          make_float4(dv_acc[r][c4], dv_acc[r][c4 + 1], dv_acc[r][c4 + 2], dv_acc[r][c4 + 3]);
+      *reinterpret_cast<float4*>(p.dk + off + c4) =
+          make_float4(dk_acc[r][c4] * p.scale, dk_acc[r][c4 + 1] * p.scale, dk_acc[r][c4 + 2] * p.scale,
+                      dk_acc[r][c4 + 3] * p.scale);
     }
   }
 }
 
-// Shared memory of the dQ kernel (floats): Q^T, dO^T [D][65]; per step K^T, V^T [D][33], K [32][D];
-// dS as [32 keys][65]; the CTA's nl and -D.
+// Shared memory of the dQ kernel (floats): Q^T, dO^T [D][MP]; per step K^T, V^T [D][NP], K [BN][D];
+// dS as [BN keys][MP]; the CTA's nl and -D.
 template <int D>
 constexpr int dq_smem_floats() {
-  return 2 * D * PAD_M + 2 * D * PAD_N + BW_N * D + BW_N * PAD_M + 2 * BW_M;
+  using T = F32Tile<D>;
+  return 2 * D * T::MP + 2 * D * T::NP + T::BN * D + T::BN * T::MP + 2 * T::BM;
 }
 
 template <int D>
 __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32Params p) {
-  extern __shared__ float sm[];
-  float* qt = sm;                       // [D][PAD_M]
-  float* dot = qt + D * PAD_M;          // [D][PAD_M]
-  float* kt = dot + D * PAD_M;          // [D][PAD_N]
-  float* vt = kt + D * PAD_N;           // [D][PAD_N]
-  float* kr = vt + D * PAD_N;           // [BW_N][D]
-  float* dss = kr + BW_N * D;           // [BW_N keys][PAD_M]
-  float* nl_s = dss + BW_N * PAD_M;     // [BW_M]
-  float* nd_s = nl_s + BW_M;            // [BW_M]
+  using T = F32Tile<D>;
+  constexpr int BM = T::BM, BN = T::BN, TQ = T::TQ, CW = T::CW, MP = T::MP, NP = T::NP;
+  extern __shared__ __align__(16) float sm[];
+  float* qt = sm;                       // [D][MP]
+  float* dot = qt + D * MP;             // [D][MP]
+  float* kt = dot + D * MP;             // [D][NP]
+  float* vt = kt + D * NP;              // [D][NP]
+  float* kr = vt + D * NP;              // [BN][D]
+  float* dss = kr + BN * D;             // [BN keys][MP]
+  float* nl_s = dss + BN * MP;          // [BM]
+  float* nd_s = nl_s + BM;              // [BM]
 
-  const int n_qblk = (p.Nq + BW_M - 1) / BW_M;
+  const int n_qblk = (p.Nq + BM - 1) / BM;
   const int qb = static_cast<int>(blockIdx.x % n_qblk);
   const int bh = static_cast<int>(blockIdx.x / n_qblk);
   const int b = bh / p.H, h = bh % p.H;
   const int bhkv = b * p.Hkv + h / (p.H / p.Hkv);
-  const int i0 = qb * BW_M;
-  const int qvalid = min(BW_M, p.Nq - i0);
+  const int i0 = qb * BM;
+  const int qvalid = min(BM, p.Nq - i0);
   const float* qg = p.q + (static_cast<size_t>(bh) * p.Nq + i0) * D;
   const float* dg = p.dout + (static_cast<size_t>(bh) * p.Nq + i0) * D;
-  load_transposed<D, BW_M>(qt, PAD_M, qg, qvalid);
-  load_transposed<D, BW_M>(dot, PAD_M, dg, qvalid);
-  if (threadIdx.x < BW_M) {
-    const size_t rr = static_cast<size_t>(bh) * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= i0 + BW_M
+  load_transposed<D, BM>(qt, MP, qg, qvalid);
+  load_transposed<D, BM>(dot, MP, dg, qvalid);
+  if (threadIdx.x < BM) {
+    const size_t rr = static_cast<size_t>(bh) * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= i0 + BM
     nl_s[threadIdx.x] = p.nl[rr];
     nd_s[threadIdx.x] = p.negd[rr];
   }
 
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  // score tile: query rows 4 ty .. 4 ty + 3, keys 2 tx, 2 tx + 1 of the step
-  // gradient tile: query rows 4 ty .. 4 ty + 3, columns tx * CW .. tx * CW + CW - 1
-  constexpr int CW = D / 16;
   float dq_acc[4][CW];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int c = 0; c < CW; ++c) dq_acc[r][c] = 0.f;
 
-  // keys any row of this block sees: j <= i0 + BW_M - 1 + causal_off under the mask
-  const int k_end = p.causal ? min(p.Nk, i0 + BW_M + p.causal_off) : p.Nk;
-  for (int j0 = 0; j0 < k_end; j0 += BW_N) {
-    const int kvalid = min(BW_N, p.Nk - j0);
+  // keys any row of this block sees: j <= i0 + BM - 1 + causal_off under the mask
+  const int k_end = p.causal ? min(p.Nk, i0 + BM + p.causal_off) : p.Nk;
+  for (int j0 = 0; j0 < k_end; j0 += BN) {
+    const int kvalid = min(BN, p.Nk - j0);
     __syncthreads();  // the previous step's tiles are no longer read (and the CTA's tiles are in)
     const float* kg = p.k + (static_cast<size_t>(bhkv) * p.Nk + j0) * D;
     const float* vg = p.v + (static_cast<size_t>(bhkv) * p.Nk + j0) * D;
-    load_transposed<D, BW_N>(kt, PAD_N, kg, kvalid);
-    load_transposed<D, BW_N>(vt, PAD_N, vg, kvalid);
-    load_rows<D, BW_N>(kr, kg, kvalid);
+    load_transposed<D, BN>(kt, NP, kg, kvalid);
+    load_transposed<D, BN>(vt, NP, vg, kvalid);
+    load_rows<D, BN>(kr, kg, kvalid);
     __syncthreads();
-    // S = Q K^T and dP = dO V^T for this thread's 4 x 2 block
-    float s[4][2], dp[4][2];
+    // S = Q K^T and dP = dO V^T for this thread's 4 x TQ block
+    float s[4][TQ], dp[4][TQ];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) s[r][0] = s[r][1] = dp[r][0] = dp[r][1] = 0.f;
-#pragma unroll 8
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int kk = 0; kk < TQ; ++kk) s[r][kk] = dp[r][kk] = 0.f;
+#pragma unroll 4
     for (int c = 0; c < D; ++c) {
-      float a[4], ag[4];
+      float a[4], ag[4], bk[TQ], bv[TQ];
+      lds_vec(a, qt + c * MP + 4 * ty);
+      lds_vec(ag, dot + c * MP + 4 * ty);
+      lds_vec(bk, kt + c * NP + TQ * tx);
+      lds_vec(bv, vt + c * NP + TQ * tx);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        a[r] = qt[c * PAD_M + 4 * ty + r];
-        ag[r] = dot[c * PAD_M + 4 * ty + r];
-      }
-      const float b0 = kt[c * PAD_N + 2 * tx], b1 = kt[c * PAD_N + 2 * tx + 1];
-      const float v0 = vt[c * PAD_N + 2 * tx], v1 = vt[c * PAD_N + 2 * tx + 1];
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        s[r][0] = fmaf(a[r], b0, s[r][0]);
-        s[r][1] = fmaf(a[r], b1, s[r][1]);
-        dp[r][0] = fmaf(ag[r], v0, dp[r][0]);
-        dp[r][1] = fmaf(ag[r], v1, dp[r][1]);
-      }
+        for (int kk = 0; kk < TQ; ++kk) {
+          s[r][kk] = fmaf(a[r], bk[kk], s[r][kk]);
+          dp[r][kk] = fmaf(ag[r], bv[kk], dp[r][kk]);
+        }
     }
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const int jl = 2 * tx + kk, j = j0 + jl;
+    for (int kk = 0; kk < TQ; ++kk) {
+      const int jl = TQ * tx + kk, j = j0 + jl;
+      float dsr[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int il = 4 * ty + r, i = i0 + il;
         const bool vis = j < p.Nk && i < p.Nq && (!p.causal || j <= i + p.causal_off);
         const float pr = vis ? ex2_approx(fmaf(s[r][kk], p.c, nl_s[il])) : 0.f;
-        dss[jl * PAD_M + il] = pr * (dp[r][kk] + nd_s[il]);
+        dsr[r] = pr * (dp[r][kk] + nd_s[il]);
       }
+      *reinterpret_cast<float4*>(dss + jl * MP + 4 * ty) = make_float4(dsr[0], dsr[1], dsr[2], dsr[3]);
     }
     __syncthreads();
     // dQ += dS K over the step's keys
 #pragma unroll 4
-    for (int jl = 0; jl < BW_N; ++jl) {
+    for (int jl = 0; jl < BN; ++jl) {
       float dr[4], kv[CW];
+      lds_vec(dr, dss + jl * MP + 4 * ty);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) dr[r] = dss[jl * PAD_M + 4 * ty + r];
+      for (int c4 = 0; c4 < CW; c4 += 4) {
+        float t0[4];
+        lds_vec(t0, kr + jl * D + tx * CW + c4);
 #pragma unroll
-      for (int c = 0; c < CW; ++c) kv[c] = kr[jl * D + tx * CW + c];
+        for (int e = 0; e < 4; ++e) kv[c4 + e] = t0[e];
+      }
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -369,7 +410,10 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32
     if (il >= qvalid) continue;
     const size_t off = (static_cast<size_t>(bh) * p.Nq + i0 + il) * D + tx * CW;
 #pragma unroll
-    for (int c = 0; c < CW; ++c) p.dq[off + c] = dq_acc[r][c] * p.scale;
+    for (int c4 = 0; c4 < CW; c4 += 4)
+      *reinterpret_cast<float4*>(p.dq + off + c4) =
+          make_float4(dq_acc[r][c4] * p.scale, dq_acc[r][c4 + 1] * p.scale, dq_acc[r][c4 + 2] * p.scale,
+                      dq_acc[r][c4 + 3] * p.scale);
   }
   // This grid may have started before the dK/dV grid finished; waiting for it here keeps every gradient
   // complete once this grid is, for the work that follows the backward on the stream.
