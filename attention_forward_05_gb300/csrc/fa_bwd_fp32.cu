@@ -426,8 +426,8 @@ cudaError_t launch_bwd_fp32_d(const BwdLaunch& a, const BwdF32Params& p) {
   const long long blocks = (rows * (D / 4) + 255) / 256;
   if (blocks <= 0 || blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   fa_bwd_prep_fp32_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
-      static_cast<const float*>(a.o), static_cast<const float*>(a.dout), a.lse, const_cast<float*>(p.nl),
-      const_cast<float*>(p.negd), rows, a.Nq, a.Nq_pad);
+      static_cast<const float*>(a.o), static_cast<const float*>(a.dout), a.lse, a.rowv, a.rowv2, rows, a.Nq,
+      a.Nq_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   constexpr int smem_kv = dkdv_smem_floats<D>() * 4;
