@@ -11,8 +11,8 @@
 
 namespace fa {
 
-using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, 64, 2, 4, 2, 1, false>;
-using CfgBf16D128 = FwdCfg<__nv_bfloat16, 128, 128, 2, 2, 1, 1, true>;
+using CfgBf16D64 = FwdCfg<__nv_bfloat16, 64, 64, 2, 4, 2, false>;
+using CfgBf16D128 = FwdCfg<__nv_bfloat16, 128, 128, 2, 2, 1, true>;
 
 cudaError_t launch_fwd_bf16_d64(const FwdLaunch& a) { return launch_fwd<CfgBf16D64>(a); }
 cudaError_t launch_fwd_bf16_d128(const FwdLaunch& a) { return launch_fwd<CfgBf16D128>(a); }

@@ -16,9 +16,9 @@
 
 namespace fa {
 
-using CfgDecD64 = FwdCfg<__nv_bfloat16, 64, 64, 1, 3, 3, 1>;
-using CfgDecD64OneWave = FwdCfg<__nv_bfloat16, 64, 64, 1, 2, 4, 1>;
-using CfgDecD128 = FwdCfg<__nv_bfloat16, 128, 64, 1, 2, 2, 1>;
+using CfgDecD64 = FwdCfg<__nv_bfloat16, 64, 64, 1, 3, 3>;
+using CfgDecD64OneWave = FwdCfg<__nv_bfloat16, 64, 64, 1, 2, 4>;
+using CfgDecD128 = FwdCfg<__nv_bfloat16, 128, 64, 1, 2, 2>;
 
 cudaError_t launch_fwd_decode(const FwdLaunch& a, int d, int sms) {
   if (d != 64) return launch_fwd<CfgDecD128>(a);

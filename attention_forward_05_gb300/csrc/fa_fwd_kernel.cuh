@@ -42,7 +42,7 @@
 
 namespace fa {
 
-template <typename T, int D_, int BC_, int NQT_, int STAGES_, int MINB_ = 1, int SPLIT_ = 1, bool PV2_ = false>
+template <typename T, int D_, int BC_, int NQT_, int STAGES_, int MINB_ = 1, bool PV2_ = false>
 struct FwdCfg {
   using Elem = T;
   static constexpr int D = D_;
@@ -50,7 +50,6 @@ struct FwdCfg {
   static constexpr int NQT = NQT_;
   static constexpr int STAGES = STAGES_;
   static constexpr int MINB = MINB_;    // CTAs per SM the launch bounds ask for
-  static constexpr int SPLIT = SPLIT_;  // softmax warpgroups per query tile, each owning BC/SPLIT key columns
   // PV2: the softmax hands over P in two halves (key columns [0, BC/2) first), and P V of the first
   // half is issued while the second half is still being exponentiated.
   static constexpr bool PV2 = PV2_;
@@ -76,10 +75,7 @@ struct FwdCfg {
   // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT], drain
   static constexpr int NBAR = 1 + 4 * STAGES + 4 * NQT + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
-  // exchange of partial row maxima / sums between the SPLIT warpgroups of a tile: [2 slots][NQT][SPLIT][128]
-  static constexpr int OFF_XCHG = OFF_MISC + 16;
-  static constexpr int XCHG_BYTES = SPLIT > 1 ? 2 * NQT * SPLIT * 128 * 4 : 0;
-  static constexpr int SMEM_BYTES = OFF_XCHG + XCHG_BYTES + 1024;  // + slack to align the base to 1024
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
   static constexpr int MMA_K = 32 / ESZ;                  // K of one tcgen05.mma (32 bytes)
   static constexpr int O_COL0 = NQT * BC;                 // TMEM: S_t at t*BC, O_t at O_COL0 + t*D
   static constexpr int TMEM_NEED = NQT * (BC + D);
@@ -87,14 +83,13 @@ struct FwdCfg {
                                    : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int P_COLS = BC * ESZ / 4;  // 32-bit TMEM columns of one P row
   static constexpr int P_COLS_PER_K = MMA_K * ESZ / 4;
-  static constexpr int COLS = BC / SPLIT;         // key columns of one softmax thread
-  static constexpr int PCOLS_W = P_COLS / SPLIT;  // P columns written by one softmax warpgroup
-  static constexpr int OCOLS = D / SPLIT;         // O columns rescaled and stored by one softmax warpgroup
-  static constexpr int NSMWG = NQT * SPLIT;       // softmax warpgroups
-  static constexpr int NWARPS = 4 * NSMWG + 2;
+  static constexpr int COLS = BC;         // key columns of one softmax thread (one query row)
+  static constexpr int PCOLS_W = P_COLS;  // P columns written by one softmax warpgroup
+  static constexpr int OCOLS = D;         // O columns rescaled and stored by one softmax warpgroup
+  static constexpr int NWARPS = 4 * NQT + 2;
   static constexpr int NTHREADS = 32 * NWARPS;
-  static constexpr int LOAD_WARP = 4 * NSMWG;
-  static constexpr int MMA_WARP = 4 * NSMWG + 1;
+  static constexpr int LOAD_WARP = 4 * NQT;
+  static constexpr int MMA_WARP = 4 * NQT + 1;
   // Registers per thread: each of the SM's 4 sub-partitions holds 16384 registers and
   // ceil(warps per SM / 4) warps, in 8-register steps.
   static constexpr int WARPS_PER_SUBPART = (NWARPS * MINB + 3) / 4;
@@ -102,9 +97,8 @@ struct FwdCfg {
   static constexpr int MAXREG = MAXREG_RAW > 248 ? 248 : MAXREG_RAW;
   static_assert(D % CHUNK == 0, "head dim must be a whole number of 128-byte segments");
   static_assert(BC % 32 == 0 && BC >= 32 && BC <= 256, "key tile");
-  static_assert(COLS % 32 == 0 && PCOLS_W % 32 == 0 && OCOLS % 32 == 0, "split into whole 32-column chunks");
-  static_assert(NQT <= 8, "one named barrier per tile");
-  static_assert(!PV2 || (SPLIT == 1 && !TF32 && BC >= 128 && (BC / 2) % 64 == 0), "P handed over in two halves of whole packed chunks");
+  static_assert(COLS % 32 == 0 && PCOLS_W % 32 == 0 && OCOLS % 32 == 0, "whole 32-column chunks");
+  static_assert(!PV2 || (!TF32 && BC >= 128 && (BC / 2) % 64 == 0), "P handed over in two halves of whole packed chunks");
   static_assert(TMEM_NEED <= 512 / MINB, "tensor memory");
   static_assert(SMEM_BYTES * MINB <= 227 * 1024, "shared memory");
 };
@@ -267,7 +261,7 @@ __global__ void __maxnreg__(C::MAXREG)
     }
     for (int t = 0; t < C::NQT; ++t) {
       mbar_init(bar_sf(t), 1);
-      mbar_init(bar_pf(t), 4 * C::SPLIT);  // one arrive per softmax warp of the tile
+      mbar_init(bar_pf(t), 4);  // one arrive per softmax warp of the tile
       mbar_init(bar_ph(t), 4);
       mbar_init(bar_od(t), 1);
     }
@@ -461,19 +455,14 @@ __global__ void __maxnreg__(C::MAXREG)
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    // Warpgroup g = warp / 4 owns query tile t = g / SPLIT and key columns
-    // [h * COLS, (h + 1) * COLS) of every key tile, h = g % SPLIT; thread = query row.
-    const int g = warp >> 2;
-    const int t = g / C::SPLIT;
-    const int h = g % C::SPLIT;
+    // Warpgroup t = warp / 4 owns query tile t; thread = query row.
+    const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_base + t * C::BC + h * C::COLS;
-    const uint32_t tP = tmem + lane_base + t * C::BC + h * C::PCOLS_W;
-    const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::D + h * C::OCOLS;
-    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCHG);
-    auto xidx = [&](int slot, int hh) { return ((slot * C::NQT + t) * C::SPLIT + hh) * 128 + row; };
+    const uint32_t tS = tmem + lane_base + t * C::BC;
+    const uint32_t tP = tmem + lane_base + t * C::BC;
+    const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::D;
     // keys this row may see in the CTA's range: [k_begin, row_lim)
     const int row_lim = p.causal ? min(k_end, q0 + t * C::BR + row + 1 + p.causal_off) : k_end;
     const float c = p.c;
@@ -486,8 +475,8 @@ __global__ void __maxnreg__(C::MAXREG)
     for (int j = 0; j < Tt; ++j) {
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
       okw = __all_sync(0xffffffffu, okw);
-      const int valid = row_lim - k_begin - j * C::BC - h * C::COLS;  // valid key columns here (may be <= 0)
-      if constexpr (C::SPLIT == 1 && !C::TF32 && C::COLS <= 64) {
+      const int valid = row_lim - k_begin - j * C::BC;  // valid key columns here (may be <= 0)
+      if constexpr (!C::TF32 && C::COLS <= 64) {
         // Fast path once every row of the warp has a reference maximum: P is computed against m_ref
         // while the scores are still arriving, 32 columns at a time (the load of the next chunk
         // overlaps the work on this one).  No row maximum is formed: the row sum bounds every P of
@@ -613,7 +602,7 @@ __global__ void __maxnreg__(C::MAXREG)
       }
       // 64-column bf16 tiles: the general path works on one 32-column chunk at a time (the maximum, then
       // P chunk by chunk), which halves the registers it holds; P and the row sum come out the same.
-      constexpr bool CHUNKED = !C::TF32 && !C::PV2 && C::SPLIT == 1 && C::COLS == 64;
+      constexpr bool CHUNKED = !C::TF32 && !C::PV2 && C::COLS == 64;
       uint32_t sr[CHUNKED ? 1 : C::COLS / 32][32];
       float m_part = -INFINITY;
       if constexpr (CHUNKED) {
@@ -655,21 +644,8 @@ __global__ void __maxnreg__(C::MAXREG)
           m_part = (c >= 0.f ? row_extreme<C::COLS, true>(sr) : row_extreme<C::COLS, false>(sr)) * c;
         }
       }
-      float m_tile = m_part;
-      if constexpr (C::SPLIT > 1) {
-        // Exchange the partial maxima (double-buffered by step parity) and agree on continuing:
-        // the barrier's AND-reduction gives every thread of the tile the same decision, so the
-        // warpgroups of a tile always meet the same number of times.
-        xch[xidx(j & 1, h)] = m_part;
-        tc_fence_before();
-        ok = bar_red_and(1 + t, 128 * C::SPLIT, okw);
-        tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < C::SPLIT; ++hh)
-          if (hh != h) m_tile = fmaxf(m_tile, xch[xidx(j & 1, hh)]);
-      } else {
-        ok = okw;
-      }
+      const float m_tile = m_part;
+      ok = okw;
       if (!ok) break;
       const float m_new = fmaxf(m_ref, m_tile);
       const bool need = m_new > m_ref + p.tau;  // always true on the first tile (m_ref = -inf)
@@ -782,35 +758,25 @@ __global__ void __maxnreg__(C::MAXREG)
       l = l * alpha + ((r0 + r1) + (r2 + r3));
     }
     // ---------------------------------------------------------- epilogue: O / l, LSE
-    if (ok && Tt > 0) {  // `ok` agrees across the warpgroups of the tile here
+    if (ok && Tt > 0) {
       bool okw = mbar_wait(bar_od(t), 0, abort_flag, p.err, W_OD);
-      okw = __all_sync(0xffffffffu, okw);
-      if constexpr (C::SPLIT > 1) {  // total row sum from the partial sums (slot Tt & 1 is free)
-        xch[xidx(Tt & 1, h)] = l;
-        ok = bar_red_and(1 + t, 128 * C::SPLIT, okw);
-        float lt = 0.f;
-#pragma unroll
-        for (int hh = 0; hh < C::SPLIT; ++hh) lt += xch[xidx(Tt & 1, hh)];
-        l = lt;
-      } else {
-        ok = okw;
-      }
+      ok = __all_sync(0xffffffffu, okw);
     }
     if (Tt == 0) {  // split mode, key range entirely above the tile's causal diagonal: empty state (-inf, 0, 0)
       const int qrow = q0 + t * C::BR + row;
       if (qrow < p.Nq) {
         const size_t srow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + qrow;
-        float* wrow = p.ws_o + srow * C::D + h * C::OCOLS;
+        float* wrow = p.ws_o + srow * C::D;
 #pragma unroll
         for (int c4 = 0; c4 < C::OCOLS / 4; ++c4) reinterpret_cast<uint4*>(wrow)[c4] = make_uint4(0, 0, 0, 0);
-        if (h == 0) reinterpret_cast<float2*>(p.ws_ml)[srow] = make_float2(-INFINITY, 0.f);
+        reinterpret_cast<float2*>(p.ws_ml)[srow] = make_float2(-INFINITY, 0.f);
       }
     } else if (ok && p.n_split > 1) {  // partial state (m, l, unnormalised O) of this key range, for the merge
       tc_fence_after();
       const int qrow = q0 + t * C::BR + row;
       const bool in_range = qrow < p.Nq;
       const size_t srow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + qrow;
-      float* wrow = p.ws_o + srow * C::D + h * C::OCOLS;
+      float* wrow = p.ws_o + srow * C::D;
 #pragma unroll
       for (int cc = 0; cc < C::OCOLS / 32; ++cc) {
         uint32_t orr[32];
@@ -823,14 +789,13 @@ __global__ void __maxnreg__(C::MAXREG)
           for (int v4 = 0; v4 < 8; ++v4) dst[v4] = make_uint4(orr[4 * v4], orr[4 * v4 + 1], orr[4 * v4 + 2], orr[4 * v4 + 3]);
         }
       }
-      if (h == 0 && in_range) reinterpret_cast<float2*>(p.ws_ml)[srow] = make_float2(m_ref, l);
+      if (in_range) reinterpret_cast<float2*>(p.ws_ml)[srow] = make_float2(m_ref, l);
     } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       const int qrow = q0 + t * C::BR + row;
       const bool in_range = qrow < p.Nq;
-      uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * C::ESZ) +
-                      h * C::OCOLS * C::ESZ;
+      uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * C::ESZ);
 #pragma unroll
       for (int cc = 0; cc < C::OCOLS / 32; ++cc) {
         uint32_t orr[32];
@@ -863,7 +828,7 @@ __global__ void __maxnreg__(C::MAXREG)
           }
         }
       }
-      if (h == 0 && p.lse != nullptr && in_range)
+      if (p.lse != nullptr && in_range)
         p.lse[static_cast<size_t>(bh) * p.Nq + qrow] = (m_ref + log2f(l)) * 0.6931471805599453f;
     }
   }

@@ -88,19 +88,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
   return true;
 }
 
-// Named barrier `id` over `nthreads` threads (whole warps) that also returns the AND of
-// every participant's predicate.
-__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
