@@ -45,14 +45,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     """Compile (if stale or forced) and return the path of libfa.so.
 
     FA_PTXAS_VERBOSE=1 in the environment adds ``-Xptxas -v`` and keeps its
-    register / spill report in _build/ptxas.log.  FA_NVCC_EXTRA adds compiler
-    flags (for experiments outside the library's own configuration); a build
-    with different extra flags is always redone.
+    register / spill report in _build/ptxas.log.
     """
-    extra = os.environ.get("FA_NVCC_EXTRA", "").split()
-    stamp = os.path.join(OUT, "flags.txt")
-    prev = open(stamp).read() if os.path.exists(stamp) else ""
-    if not force and not is_stale() and prev == " ".join(extra):
+    if not force and not is_stale():
         return LIB
     os.makedirs(OUT, exist_ok=True)
     nvcc = _nvcc()
@@ -61,7 +56,6 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     "--expt-relaxed-constexpr"]
     if ptxas_v:
         flags += ["-Xptxas", "-v"]
-    flags += extra
 
     def compile_one(src: str):
         obj = os.path.join(OUT, src.replace(".cu", ".o"))
@@ -87,8 +81,6 @@ def build(force: bool = False, verbose: bool = False) -> str:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc link failed")
     os.replace(tmp, LIB)
-    with open(stamp, "w") as f:
-        f.write(" ".join(extra))
     return LIB
 
 
