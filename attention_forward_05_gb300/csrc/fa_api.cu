@@ -200,6 +200,28 @@ int plan_fwd(int B, int H, int Hkv, int Nq, int Nk, int d, int dtype, int causal
   return FA_OK;
 }
 
+// The last, partial wave of a d = 64 bf16 forward without mask or key splits.  When the CTA units (256
+// query rows) do not fill whole waves of two CTAs per SM and what is left is at most one CTA per SM,
+// those CTAs would each run alone on an SM through all the key tiles.  Their rows are taken instead by
+// key-split CTAs: one 128-row query tile each, its two tile slots over the two halves of the keys,
+// merged inside the CTA at the end (twice as many CTAs, chains of half the length).
+void plan_key_split(long long BH, int Nq, int Nk, int sms, const fa::FwdGeometry& geo, fa::FwdLaunch* a) {
+  if (sms <= 0 || geo.rows_per_cta != 256 || geo.ctas_per_sm != 2 || geo.kv_rows != 64) return;
+  const long long per_head = (Nq + 255) / 256, per_head1 = (Nq + 127) / 128;
+  const long long units = per_head * BH, slots = 2LL * sms;
+  const long long rest = units % slots;
+  const long long tiles = (Nk + 63) / 64;
+  if (units < slots || rest == 0 || rest > sms || tiles < 8) return;
+  const long long u0 = units - rest;  // first unit of the last wave: head u0 / per_head, block u0 % per_head
+  const long long first = (u0 / per_head) * per_head1 + 2 * (u0 % per_head);
+  const long long count = BH * per_head1 - first;
+  if (u0 + count > 0x7FFFFFFFLL) return;
+  a->ks_whole = static_cast<int>(u0);
+  a->ks_tile0 = static_cast<int>(first);
+  a->ks_count = static_cast<int>(count);
+  a->ks_half = static_cast<int>((tiles + 1) / 2 * 64);
+}
+
 }  // namespace
 
 extern "C" {
@@ -295,6 +317,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.fault = g_fault.exchange(0);
   a.stream = st;
   a.dependent = geo.v_kmajor ? 1 : 0;  // the fp32 prep kernel was the last launch on `st`
+  if (bf16 && d == 64 && !causal && kv_splits == 0 && pl.n_split == 1) plan_key_split(BH, Nq, Nk, sms, geo, &a);
   cudaError_t e;
   if (bf16)
     e = (d == 64) ? fa::launch_fwd_bf16_d64(a) : fa::launch_fwd_bf16_d128(a);

@@ -75,7 +75,12 @@ struct FwdCfg {
   // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT], drain
   static constexpr int NBAR = 1 + 4 * STAGES + 4 * NQT + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem slot (4 B) + abort flag (4 B)
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  // Key-split CTAs (FwdParams::ks_half) exist for the two-tile bf16 configuration without the two-half
+  // hand-over; their tile slot 1 leaves its rows' (m, l) here for the merge.
+  static constexpr bool KS = NQT == 2 && !TF32 && !PV2;
+  static constexpr int OFF_ML = OFF_MISC + 16;
+  static constexpr int ML_BYTES = KS ? BR * 8 : 0;
+  static constexpr int SMEM_BYTES = OFF_ML + ML_BYTES + 1024;  // + slack to align the base to 1024
   static constexpr int MMA_K = 32 / ESZ;                  // K of one tcgen05.mma (32 bytes)
   static constexpr int O_COL0 = NQT * BC;                 // TMEM: S_t at t*BC, O_t at O_COL0 + t*D
   static constexpr int TMEM_NEED = NQT * (BC + D);
@@ -118,6 +123,11 @@ struct FwdParams {
   float c, tau;
   float p_lim;          // 2^tau: largest row sum of P that proves no maximum moved past m_ref + tau
   int fault;
+  // Key-split CTAs (no mask, n_split == 1; ks_half = 0: none).  CTAs below n_whole are the usual ones;
+  // CTA n_whole + i takes one 128-row query tile, number ks_tile0 + i of the head-major list of 128-row
+  // tiles, and gives its two tile slots the keys [0, ks_half) and [ks_half, Nk); at the end slot 0
+  // merges the two partial states (both in this CTA's tensor memory) and writes O and the LSE.
+  int n_whole, ks_tile0, ks_half;
 };
 
 // wait-site identifiers recorded with a timeout
@@ -212,30 +222,46 @@ __global__ void __maxnreg__(C::MAXREG)
   // are adjacent.  With a causal mask a CTA's work grows with its query block, so the query block is
   // the slowest index, last block first: blockIdx.x = (n_qblk - 1 - qb) * (n_split * BH) + split * BH
   // + bh.  The longest CTAs start first and the shortest fill the last wave.
-  int qb, bh, split;
+  int qb, bh, split, q0;
+  // a key-split CTA (FwdParams): both tile slots hold the same 128 query rows, over two key ranges
+  const bool ks = C::KS && p.ks_half > 0 && static_cast<int>(blockIdx.x) >= p.n_whole;
   if (p.causal) {
     const int per_qb = p.n_split * p.BH;
     qb = p.n_qblk - 1 - static_cast<int>(blockIdx.x / per_qb);
     bh = static_cast<int>(blockIdx.x % per_qb) % p.BH;
     split = static_cast<int>(blockIdx.x % per_qb) / p.BH;
+    q0 = qb * C::BR * C::NQT;
+  } else if (ks) {
+    const int nq1 = (p.Nq + C::BR - 1) / C::BR;
+    const int tile = p.ks_tile0 + static_cast<int>(blockIdx.x) - p.n_whole;
+    bh = tile / nq1;
+    qb = 0;
+    split = 0;
+    q0 = (tile % nq1) * C::BR;
   } else {
     qb = static_cast<int>(blockIdx.x % p.n_qblk);
     bh = static_cast<int>(blockIdx.x / p.n_qblk) % p.BH;
     split = static_cast<int>(blockIdx.x / (p.n_qblk * p.BH));
+    q0 = qb * C::BR * C::NQT;
   }
   const int kvh = (bh / p.H) * p.Hkv + (bh % p.H) / (p.H / p.Hkv);  // key/value head of this query head
-  const int q0 = qb * C::BR * C::NQT;
   const int k_begin = split * p.kv_per_split;
   const int k_end = min(p.Nk, k_begin + p.kv_per_split);  // the host makes every split non-empty
   // keys past the causal limit of the CTA's last row are never loaded or multiplied
   const int k_hi = p.causal ? min(k_end, q0 + C::NQT * C::BR + p.causal_off) : k_end;
-  const int T = k_hi > k_begin ? (k_hi - k_begin + C::BC - 1) / C::BC : 0;  // 0 only in split mode
+  // key range of tile slot t (the CTA's range, or one of the two halves in a key-split CTA)
+  auto slot_lo = [&](int t) { return ks && t == 1 ? p.ks_half : k_begin; };
+  auto slot_hi = [&](int t) { return ks && t == 0 ? min(k_end, p.ks_half) : k_end; };
+  const int T = ks ? (slot_hi(0) + C::BC - 1) / C::BC
+                   : (k_hi > k_begin ? (k_hi - k_begin + C::BC - 1) / C::BC : 0);  // 0 only in split mode
   // Key tiles query tile t needs: with a causal mask the tiles past its own last row's limit are
   // skipped (no products, no softmax); the last tile needs all T.
   auto tile_steps = [&](int t) {
+    if (ks) return (slot_hi(t) - slot_lo(t) + C::BC - 1) / C::BC;
     const int hi = p.causal ? min(k_end, q0 + (t + 1) * C::BR + p.causal_off) : k_end;
     return hi > k_begin ? (hi - k_begin + C::BC - 1) / C::BC : 0;
   };
+  const int trow = ks ? 0 : C::BR;  // rows of tile slot t start at q0 + t * trow
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_q = bar0;
@@ -298,8 +324,39 @@ __global__ void __maxnreg__(C::MAXREG)
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(sbase + C::OFF_Q + t * C::Q_BYTES + c * C::Q_CH_BYTES, &tm_q, bar_q, c * C::CHUNK,
-                      q0 + t * C::BR, bh);
-      for (int j = 0; j < T; ++j) {
+                      q0 + t * trow, bh);
+      if constexpr (C::KS) {
+        if (ks) {
+          // Copy n = 2j + t is key tile j of slot t (slot 1 may have one tile fewer): ring stage n % STAGES.
+          const int T1 = tile_steps(1);
+          int n = 0;
+          for (int j = 0; j < T; ++j) {
+            for (int t = 0; t < 2; ++t) {
+              if (t == 1 && j >= T1) break;
+              const int s = n % C::STAGES;
+              const uint32_t ph = ((n / C::STAGES) & 1) ^ 1;
+              const int key = slot_lo(t) + j * C::BC;
+              if (!mbar_wait(bar_ke(s), ph, abort_flag, p.err, W_KE)) goto ks_loads_done;
+              mbar_expect_tx(bar_kf(s), C::KV_BYTES);
+#pragma unroll
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_3d(sbase + C::OFF_K + s * C::KV_BYTES + c * C::KV_CH_BYTES, &tm_k, bar_kf(s), c * C::CHUNK,
+                            key, kvh);
+              nk_done = n + 1;
+              if (!mbar_wait(bar_ve(s), ph, abort_flag, p.err, W_VE)) goto ks_loads_done;
+              mbar_expect_tx(bar_vf(s), C::KV_BYTES);
+#pragma unroll
+              for (int c = 0; c < C::NCH_V; ++c)
+                tma_load_3d(sbase + C::OFF_V + s * C::KV_BYTES + c * C::V_CH_BYTES, &tm_v, bar_vf(s), c * C::CHUNK,
+                            key, kvh);
+              nv_done = n + 1;
+              ++n;
+            }
+          }
+        ks_loads_done:;
+        }
+      }
+      for (int j = 0; !ks && j < T; ++j) {
         const int s = j % C::STAGES;
         const uint32_t ph = ((j / C::STAGES) & 1) ^ 1;
         if (!mbar_wait(bar_ke(s), ph, abort_flag, p.err, W_KE)) break;
@@ -330,7 +387,7 @@ __global__ void __maxnreg__(C::MAXREG)
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) {
         int nks = (nk_done > s) ? (nk_done - 1 - s) / C::STAGES + 1 : 0;
-        if (p.fault == 1 && s == 0 && nk_done > 0) --nks;  // the skipped copy of tile 0
+        if (!ks && p.fault == 1 && s == 0 && nk_done > 0) --nks;  // the skipped copy of tile 0
         const int nvs = (nv_done > s) ? (nv_done - 1 - s) / C::STAGES + 1 : 0;
         if (nks > 0) mbar_wait_drain(bar_kf(s), (nks - 1) & 1, p.err, W_DRAIN_K);
         if (nvs > 0) mbar_wait_drain(bar_vf(s), (nvs - 1) & 1, p.err, W_DRAIN_V);
@@ -387,6 +444,49 @@ __global__ void __maxnreg__(C::MAXREG)
         if (elect_one()) mma_commit(bar);
         __syncwarp();
       };
+      if (C::KS && ks) {
+        // Key-split CTA: slot t's key tile j is copy n = 2j + t of the ring (stage n % STAGES); each
+        // stage serves one slot, so it is released after that slot's products.
+        const int T1 = tile_steps(1);
+        bool ok = wait_all(bar_q, 0, W_Q);
+        for (int t = 0; ok && t < 2; ++t) {  // the first Q K^T of each slot: copies 0 and 1
+          ok = wait_all(bar_kf(t % C::STAGES), (t / C::STAGES) & 1, W_KF);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+            issue_qk(t, t % C::STAGES);
+            mma_commit(bar_sf(t));
+            mma_commit(bar_ke(t % C::STAGES));
+          }
+          __syncwarp();
+        }
+        for (int j = 0; ok && j < T; ++j) {
+          for (int t = 0; t < 2; ++t) {
+            const int Tt = t == 0 ? T : T1;
+            if (j >= Tt) break;
+            const int n = 2 * j + t, s = n % C::STAGES;
+            const int n1 = n + 2, s1 = n1 % C::STAGES;
+            const bool next = j + 1 < Tt;
+            ok = wait_all(bar_vf(s), (n / C::STAGES) & 1, W_VF);
+            if (ok && next) ok = wait_all(bar_kf(s1), (n1 / C::STAGES) & 1, W_KF);
+            if (ok) ok = wait_all(bar_pf(t), j & 1, W_PF);
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
+              issue_pv(t, s, j > 0);
+              mma_commit(bar_ve(s));
+              if (next) {
+                issue_qk(t, s1);
+                mma_commit(bar_sf(t));
+                mma_commit(bar_ke(s1));
+              } else {
+                mma_commit(bar_od(t));
+              }
+            }
+            __syncwarp();
+          }
+        }
+      } else {
       bool ok = T > 0 && wait_all(bar_q, 0, W_Q) && wait_all(bar_kf(0), 0, W_KF);
       if (ok) {
         tc_fence_after();
@@ -449,6 +549,7 @@ __global__ void __maxnreg__(C::MAXREG)
           __syncwarp();
         }
       }
+      }
       // Drain: all MMAs issued above complete before tensor memory is freed.
       commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, p.err, W_DRAIN_MMA);
@@ -464,7 +565,8 @@ __global__ void __maxnreg__(C::MAXREG)
     const uint32_t tP = tmem + lane_base + t * C::BC;
     const uint32_t tO = tmem + lane_base + C::O_COL0 + t * C::D;
     // keys this row may see in the CTA's range: [k_begin, row_lim)
-    const int row_lim = p.causal ? min(k_end, q0 + t * C::BR + row + 1 + p.causal_off) : k_end;
+    const int row_lim = p.causal ? min(k_end, q0 + t * C::BR + row + 1 + p.causal_off) : slot_hi(t);
+    const int kb = slot_lo(t);
     const float c = p.c;
     float m_ref = -INFINITY;
     float l = 0.f;
@@ -475,7 +577,7 @@ __global__ void __maxnreg__(C::MAXREG)
     for (int j = 0; j < Tt; ++j) {
       bool okw = mbar_wait(bar_sf(t), j & 1, abort_flag, p.err, W_SF);
       okw = __all_sync(0xffffffffu, okw);
-      const int valid = row_lim - k_begin - j * C::BC;  // valid key columns here (may be <= 0)
+      const int valid = row_lim - kb - j * C::BC;  // valid key columns here (may be <= 0)
       if constexpr (!C::TF32 && C::COLS <= 64) {
         // Fast path once every row of the warp has a reference maximum: P is computed against m_ref
         // while the scores are still arriving, 32 columns at a time (the load of the next chunk
@@ -762,8 +864,51 @@ __global__ void __maxnreg__(C::MAXREG)
       bool okw = mbar_wait(bar_od(t), 0, abort_flag, p.err, W_OD);
       ok = __all_sync(0xffffffffu, okw);
     }
-    if (Tt == 0) {  // split mode, key range entirely above the tile's causal diagonal: empty state (-inf, 0, 0)
-      const int qrow = q0 + t * C::BR + row;
+    if (C::KS && ks) {
+      // Key-split CTA: slot 1 leaves its rows' (m, l) in shared memory; slot 0 merges the two partial
+      // states (both O in this CTA's tensor memory, on the same lanes) in key order and writes O and the
+      // LSE ("CS349E 第 11 讲 01_online_softmax.py", demo 2: partial states merge by rescaling to the
+      // larger maximum).  Every thread of both warpgroups reaches the barrier.
+      float2* ml1 = reinterpret_cast<float2*>(smem + C::OFF_ML);
+      if (t == 1 && ok) ml1[row] = make_float2(m_ref, l);
+      tc_fence_before();
+      named_bar_sync(1, 2 * C::BR);
+      const int qrow = q0 + row;
+      const bool in_range = qrow < p.Nq;
+      if (t == 0 && ok) {  // warp-uniform: the TMEM loads below are warp-collective; only stores are per row
+        tc_fence_after();
+        const float2 o1 = ml1[row];
+        const float M = fmaxf(m_ref, o1.x);
+        const float a0 = ex2_approx(m_ref - M), a1 = ex2_approx(o1.x - M);
+        const float L = fmaf(o1.y, a1, l * a0);
+        const float inv_l = 1.f / L;
+        const float w0 = a0 * inv_l, w1 = a1 * inv_l;
+        uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * C::ESZ);
+        const uint32_t tO1 = tO + C::D;  // slot 1's O: the next D columns, same lanes
+#pragma unroll
+        for (int cc = 0; cc < C::OCOLS / 16; ++cc) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16x(tO + cc * 16, r0);
+          tmem_ld16x(tO1 + cc * 16, r1);
+          tmem_wait_ld();
+          reg_fence(r0);
+          reg_fence(r1);
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_bf16x2(fmaf(__uint_as_float(r1[2 * e]), w1, __uint_as_float(r0[2 * e]) * w0),
+                               fmaf(__uint_as_float(r1[2 * e + 1]), w1, __uint_as_float(r0[2 * e + 1]) * w0));
+          if (in_range) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 16 * 2);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+        if (p.lse != nullptr && in_range)
+          p.lse[static_cast<size_t>(bh) * p.Nq + qrow] = (M + log2f(L)) * 0.6931471805599453f;
+      }
+    } else if (Tt == 0) {  // split mode, key range entirely above the tile's causal diagonal: empty state (-inf, 0, 0)
+      const int qrow = q0 + t * trow + row;
       if (qrow < p.Nq) {
         const size_t srow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + qrow;
         float* wrow = p.ws_o + srow * C::D;
@@ -773,7 +918,7 @@ __global__ void __maxnreg__(C::MAXREG)
       }
     } else if (ok && p.n_split > 1) {  // partial state (m, l, unnormalised O) of this key range, for the merge
       tc_fence_after();
-      const int qrow = q0 + t * C::BR + row;
+      const int qrow = q0 + t * trow + row;
       const bool in_range = qrow < p.Nq;
       const size_t srow = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + qrow;
       float* wrow = p.ws_o + srow * C::D;
@@ -793,7 +938,7 @@ __global__ void __maxnreg__(C::MAXREG)
     } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const int qrow = q0 + t * C::BR + row;
+      const int qrow = q0 + t * trow + row;
       const bool in_range = qrow < p.Nq;
       uint8_t* orow = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qrow) * (C::D * C::ESZ);
 #pragma unroll
@@ -869,10 +1014,25 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   p.tau = a.tau;
   p.p_lim = exp2f(a.tau);
   p.fault = a.fault;
+  p.n_whole = 0;
+  p.ks_tile0 = 0;
+  p.ks_half = 0;
+  if (a.ks_half > 0) {
+    // key-split CTAs after ks_whole usual ones: the configuration must have them, no mask, one split, and
+    // both key halves non-empty (the first a whole number of key tiles)
+    const long long nq1 = (static_cast<long long>(a.Nq) + C::BR - 1) / C::BR;
+    if (!C::KS || a.causal || a.n_split != 1 || a.ks_half % C::BC != 0 || a.ks_half >= a.Nk || a.ks_whole < 0 ||
+        a.ks_tile0 < 0 || a.ks_count < 1 || static_cast<long long>(a.ks_tile0) + a.ks_count > nq1 * a.BH)
+      return cudaErrorInvalidValue;
+    p.n_whole = a.ks_whole;
+    p.ks_tile0 = a.ks_tile0;
+    p.ks_half = a.ks_half;
+  }
   if (a.n_split < 1 || a.kv_per_split < C::BC || a.kv_per_split % C::BC != 0 ||
       static_cast<long long>(a.n_split - 1) * a.kv_per_split >= a.Nk)
     return cudaErrorInvalidValue;  // every split must own at least one key
-  const long long grid = static_cast<long long>(p.n_qblk) * a.BH * a.n_split;
+  long long grid = static_cast<long long>(p.n_qblk) * a.BH * a.n_split;
+  if (a.ks_half > 0) grid = static_cast<long long>(a.ks_whole) + a.ks_count;
   if (grid <= 0 || grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   if (a.dependent)
     return launch_dependent(fa_fwd_kernel<C>, static_cast<unsigned>(grid), C::NTHREADS, C::SMEM_BYTES, a.stream,

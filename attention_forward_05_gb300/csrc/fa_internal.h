@@ -62,6 +62,11 @@ struct FwdLaunch {
   int fault;                // test-only fault injection mode (0 = none)
   cudaStream_t stream;
   int dependent = 0;        // 1: the fp32 prep kernel precedes it on `stream` (programmatic dependent launch)
+  // Key-split CTAs (bf16, d = 64, no mask, n_split == 1; ks_half = 0: none): the grid is ks_whole usual
+  // CTAs (units 0 .. ks_whole - 1) and then ks_count CTAs of one 128-row query tile each (tiles
+  // ks_tile0 .. of the head-major list of 128-row tiles), whose two tile slots take the keys [0, ks_half)
+  // and [ks_half, Nk) and merge (fa_fwd_kernel.cuh, FwdParams).
+  int ks_whole = 0, ks_tile0 = 0, ks_count = 0, ks_half = 0;
 };
 
 // Tile geometry the tensor maps must be encoded with, per instantiation.

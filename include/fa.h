@@ -92,6 +92,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *              applied to every query row).  Automatic splitting is used only
  *              when the query tiles alone cannot fill the GPU.  n may not exceed
  *              the number of key tiles (FA_ERR_INVALID_ARG).
+ *              Automatic mode also shortens a short last wave (bf16, d = 64, no
+ *              mask): when the CTAs of 256 query rows do not fill whole waves of
+ *              two per SM and the rest is at most one per SM, the rows of that
+ *              rest go to CTAs of 128 rows whose two halves of the keys run side
+ *              by side and merge inside the CTA ([T3] demo 2).  No workspace; the
+ *              result depends only on the shape and the GPU's SM count.
+ *              kv_splits = 1 keeps every CTA on the whole key range.
  *   workspace  device buffer of at least fa_fwd_workspace_bytes(...) bytes,
  *              16-byte aligned, or NULL to allocate it stream-ordered.  Needed
  *              by the fp32 path (rounded / transposed operand copies) and by
