@@ -25,10 +25,6 @@
 // With NQT = 2 the two query tiles ping-pong: while warpgroup 0 does the
 // softmax of step j the tensor core computes tile 1's products, and vice versa
 // ([T3] demo 3 remark on FA3-style ping-pong of softmax and MMA).
-// A key-split CTA (FwdParams::ks_half) gives its two tile slots the same 128
-// query rows and the two halves of the keys instead, and merges the two
-// partial states at the end ([T3] demo 2): the short last wave of a launch
-// then runs chains of half the length.
 //
 // Lazy rescale: a row's reference maximum m_ref only moves when the new
 // maximum exceeds it by more than tau (log2 units).  P = 2^(t - m_ref) then
