@@ -81,3 +81,20 @@ def test_key_split_repeatable(cuda_device):
     for _ in range(3):
         o, lse = _fwd(q, k, v, w.scale)
         assert torch.equal(o, o0) and torch.equal(lse, l0)
+
+
+def test_key_split_without_lse_and_on_a_stream(cuda_device):
+    """Key-split CTAs with no LSE output, into a caller's O, on a side stream: the same O as with the
+    LSE on the default stream."""
+    B, H, N = 1, 20, 4096
+    q, k, v = make_qkv(B, H, N, N, 64, "bf16", seed=5400, device=cuda_device)
+    o_ref, _ = _fwd(q, k, v, 0.125)
+    o = torch.full_like(q, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _, lse = fa.fa_fwd(q, k, v, scale=0.125, o=o, with_lse=False, stream=s)
+    s.synchronize()
+    assert lse is None
+    assert fa.fa_check_device_error() == fa.FA_OK
+    assert torch.equal(o, o_ref)
