@@ -122,6 +122,9 @@ def _dtype_code(t: torch.Tensor) -> int:
 def _need_cuda_contig(name: str, t: torch.Tensor) -> None:
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device and encodes its tensor maps there
+        raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
