@@ -13,14 +13,12 @@ namespace fa {
 // dQ: two 128-row query tiles per CTA, 64 keys per step; K/V rings of 6 stages at d = 64 (+0.8% over 4)
 // and 3 at d = 128 (+1.7% over 2).
 // d=64 uses three score slots in TMEM (512 columns), d=128 two (its dV and dK take 256).
-// HALF (d = 128 only): the gradient (dV, dK) or dQ MMAs of a step start once the first half of its
-// columns is written (+4.6%; 1-2% slower at d = 64).
 // ATMEM (d = 64 only: tensor memory has no room at d = 128): the dQ kernel's S and dP MMAs take Q and
 // dO from tensor memory.
-using BwdKV64 = BwdKVCfg<64, 64, 8, 3, false>;
-using BwdKV128 = BwdKVCfg<128, 64, 4, 2, true>;
-using BwdQ64 = BwdQCfg<64, 64, 6, false, true>;
-using BwdQ128 = BwdQCfg<128, 64, 3, true>;
+using BwdKV64 = BwdKVCfg<64, 64, 8, 3>;
+using BwdKV128 = BwdKVCfg<128, 64, 4, 2>;
+using BwdQ64 = BwdQCfg<64, 64, 6, true>;
+using BwdQ128 = BwdQCfg<128, 64, 3, false>;
 
 // D_i = sum_c dO_ic O_ic (fp32 over the bf16 inputs) and nl_i = -L_i log2(e) for the rows of
 // [BH][Nq_pad], written interleaved by row pairs: rowv[pair] = (nl_2i, nl_2i+1, -D_2i, -D_2i+1)

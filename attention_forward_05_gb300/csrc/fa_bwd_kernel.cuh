@@ -18,11 +18,15 @@
 //                       query head that shares the key/value head, with S^T and dP^T computed key-major
 //                       (keys on the TMEM lanes), so P^T and dS^T are the tensor-memory A operands of
 //                       dV += P^T dO and dK += dS^T Q.  dV and dK stay in tensor memory throughout.
+//                       A step's warpgroup writes P^T first (dV starts on it) and forms dS^T once dP^T
+//                       has landed, while dV runs.
 //   fa_bwd_dq_kernel    one CTA per two 128-row query tiles; it walks the key tiles, recomputes S and
-//                       dP, and accumulates dQ += dS K with dS read from tensor memory.
-// Both main kernels keep the forward's warp roles: one TMA warp, one MMA-issuing warp, and
-// warpgroups of thread-per-row elementwise work that take turns, so the tensor core computes the
-// next products while a warpgroup works on the last ones.
+//                       dP, and accumulates dQ += dS K with dS read from tensor memory.  dS goes over
+//                       dP, so the next step's S is issued as soon as the warpgroup has read S (its
+//                       exponentials then overlap dQ and the next dP).
+// Both main kernels keep the forward's warp roles: one TMA warp, MMA-issuing warps, and warpgroups
+// of thread-per-row elementwise work that take turns, so the tensor core computes the next products
+// while a warpgroup works on the last ones.
 #pragma once
 
 #include "fa_internal.h"
@@ -79,14 +83,13 @@ enum : int { WB_KV = 0x21, WB_SF, WB_SE, WB_PF, WB_DONE, WB_Q, WB_KF, WB_VF, WB_
 
 // ------------------------------------------------------------------------------------------ dK, dV
 
-template <int D_, int BQ_, int STAGES_, int NSLOT_, bool HALF_ = true>
+template <int D_, int BQ_, int STAGES_, int NSLOT_>
 struct BwdKVCfg {
   static constexpr int D = D_;
   static constexpr int BK = 128;             // keys per CTA (TMEM lanes, M of every MMA)
   static constexpr int BQ = BQ_;             // query rows per step (N of S^T and dP^T, K of dV and dK)
   static constexpr int STAGES = STAGES_;     // ring of (Q_i, dO_i, row values)
   static constexpr int NSLOT = NSLOT_;       // TMEM slots for (S^T, dP^T); one elementwise warpgroup each
-  static constexpr bool HALF = HALF_;        // gradient MMAs start on the first half of a step's columns
   static constexpr int CHUNK = 64;           // bf16 elements per 128-byte swizzled row segment
   static constexpr int NCH = D / CHUNK;
   static constexpr int MMA_K = 16;
@@ -101,9 +104,10 @@ struct BwdKVCfg {
   static constexpr int OFF_DO = OFF_Q + STAGES * QS_BYTES;
   static constexpr int OFF_VEC = OFF_DO + STAGES * QS_BYTES;  // stage s at + s * VEC_BYTES
   static constexpr int OFF_BAR = OFF_VEC + STAGES * VEC_BYTES;
-  // barriers: kv_full, st_full[S], st_empty[S], s_full[NSLOT], p_full[NSLOT], g_free[NSLOT], done,
-  // drain (score issuer), drain (gradient issuer), p_half[NSLOT]
-  static constexpr int NBAR = 1 + 2 * STAGES + 4 * NSLOT + 3;
+  // barriers: kv_full, st_full[S], st_empty[S], s_full[NSLOT] (S^T complete), ds_full[NSLOT] (dS^T
+  // written), g_free[NSLOT], done, drain (score issuer), drain (gradient issuer), dp_full[NSLOT] (dP^T
+  // complete), pt_full[NSLOT] (P^T written)
+  static constexpr int NBAR = 1 + 2 * STAGES + 5 * NSLOT + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM: slot b holds S^T at b*2*BQ and dP^T at b*2*BQ + BQ; P^T and dS^T (bf16 pairs) are written
@@ -141,35 +145,28 @@ struct BwdKVParams {
   int fault;               // test only: 1 = the load warp skips the K/V copy (the waits for it run out)
 };
 
-// One step of a dK/dV elementwise thread (one key row, BQ query columns): P^T = 2^(s c - L log2 e),
-// dS^T = P^T (dP^T - D), both written back over S^T and dP^T as bf16 pairs.  rv holds the step's
-// (-L log2 e, -D) by column pairs.  MASK: columns q < qmin are above the causal diagonal (P = 0).
+// First part of a dK/dV elementwise step (thread = key row, BQ query columns): P^T = 2^(s c - L log2 e)
+// into registers (f32 pairs) and, as bf16 pairs, over the first BQ/2 columns of S^T, the A operand of
+// dV += P^T dO.  rv holds the step's (-L log2 e, -D) by column pairs.  MASK: columns q < qmin are above
+// the causal diagonal (P = 0).
 template <class C, bool MASK>
-__device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, const float4* rv, uint64_t c2, int qmin,
-                                                 uint32_t bar_half, int lane) {
-  // 16-column chunks: the TMEM loads of chunk cc + 1 are in flight while chunk cc is computed, and
-  // each chunk's 8 packed columns are stored at once (columns 8 cc .. 8 cc + 7, all read already).
+__device__ __forceinline__ void dkdv_p_first(uint32_t tS, const float4* rv, uint64_t c2, int qmin,
+                                             uint64_t (&pp)[C::BQ / 2]) {
   constexpr int NCHK = C::BQ / 16;
-  uint32_t sr[2][16], dr[2][16];
-  tmem_ld16(tS, sr[0]);
-  tmem_ld16(tdP, dr[0]);
+  uint32_t sr[NCHK][16];
+#pragma unroll
+  for (int cc = 0; cc < NCHK; ++cc) tmem_ld16(tS + cc * 16, sr[cc]);
   tmem_wait_ld();
-  reg_fence(sr[0]);
-  reg_fence(dr[0]);
+#pragma unroll
+  for (int cc = 0; cc < NCHK; ++cc) reg_fence(sr[cc]);
 #pragma unroll
   for (int cc = 0; cc < NCHK; ++cc) {
-    if (cc + 1 < NCHK) {
-      tmem_ld16(tS + (cc + 1) * 16, sr[(cc + 1) & 1]);
-      tmem_ld16(tdP + (cc + 1) * 16, dr[(cc + 1) & 1]);
-    }
-    const uint32_t(&s16)[16] = sr[cc & 1];
-    const uint32_t(&d16)[16] = dr[cc & 1];
-    uint32_t pk_p[8], pk_ds[8];
+    uint32_t pk_p[8];
 #pragma unroll
     for (int e = 0; e < 16; e += 2) {
       const int q = cc * 16 + e;
-      const float4 vv = rv[q / 2];  // (-L log2 e, -D) of columns q and q + 1
-      const uint64_t x = f2_fma(f2_pack(__uint_as_float(s16[e]), __uint_as_float(s16[e + 1])), c2,
+      const float4 vv = rv[q / 2];
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1])), c2,
                                 f2_pack(vv.x, vv.y));
       float x0, x1;
       f2_unpack_f(x, x0, x1);
@@ -178,24 +175,41 @@ __device__ __forceinline__ void dkdv_elementwise(uint32_t tS, uint32_t tdP, cons
         if (q < qmin) p0 = 0.f;
         if (q + 1 < qmin) p1 = 0.f;
       }
-      const uint64_t t = f2_add(f2_pack(__uint_as_float(d16[e]), __uint_as_float(d16[e + 1])), f2_pack(vv.z, vv.w));
-      const uint64_t ds = f2_mul(f2_pack(p0, p1), t);
-      float ds0, ds1;
-      f2_unpack_f(ds, ds0, ds1);
+      pp[q / 2] = f2_pack(p0, p1);
       pk_p[e / 2] = pack_bf16x2(p0, p1);
-      pk_ds[e / 2] = pack_bf16x2(ds0, ds1);
     }
     tmem_st8(tS + cc * 8, pk_p);
-    tmem_st8(tdP + cc * 8, pk_ds);
-    if (C::HALF && cc == NCHK / 2 - 1) {  // the first half of the step's query columns is in: the gradient MMAs may start
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_half);
+  }
+}
+
+// Second part: dS^T = P^T (dP^T - D) from the f32 P^T, as bf16 pairs over the first BQ/2 columns of dP^T,
+// the A operand of dK += dS^T Q (16-column chunks with the next chunk's TMEM load in flight; chunk cc's
+// 8 packed columns go over columns already read).
+template <class C>
+__device__ __forceinline__ void dkdv_ds_second(uint32_t tdP, const float4* rv, const uint64_t (&pp)[C::BQ / 2]) {
+  constexpr int NCHK = C::BQ / 16;
+  uint32_t dr[2][16];
+  tmem_ld16(tdP, dr[0]);
+  tmem_wait_ld();
+  reg_fence(dr[0]);
+#pragma unroll
+  for (int cc = 0; cc < NCHK; ++cc) {
+    if (cc + 1 < NCHK) tmem_ld16(tdP + (cc + 1) * 16, dr[(cc + 1) & 1]);
+    const uint32_t(&d16)[16] = dr[cc & 1];
+    uint32_t pk_ds[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+      const int q = cc * 16 + e;
+      const float4 vv = rv[q / 2];
+      const uint64_t t = f2_add(f2_pack(__uint_as_float(d16[e]), __uint_as_float(d16[e + 1])), f2_pack(vv.z, vv.w));
+      const uint64_t ds = f2_mul(pp[q / 2], t);
+      float ds0, ds1;
+      f2_unpack_f(ds, ds0, ds1);
+      pk_ds[e / 2] = pack_bf16x2(ds0, ds1);
     }
+    tmem_st8(tdP + cc * 8, pk_ds);
     if (cc + 1 < NCHK) {
       tmem_wait_ld();
-      reg_fence(sr[(cc + 1) & 1]);
       reg_fence(dr[(cc + 1) & 1]);
     }
   }
@@ -233,12 +247,13 @@ __global__ void __maxnreg__(C::MAXREG)
   auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
   auto bar_sf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + w); };
-  auto bar_pf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + C::NSLOT + w); };
+  auto bar_dsf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + C::NSLOT + w); };  // dS^T written
   auto bar_gf = [&](int w) { return bar0 + 8u * (1 + 2 * C::STAGES + 2 * C::NSLOT + w); };
   const uint32_t bar_done = bar0 + 8u * (1 + 2 * C::STAGES + 3 * C::NSLOT);
   const uint32_t bar_drain = bar_done + 8u;
   const uint32_t bar_drain_g = bar_done + 16u;
-  auto bar_ph = [&](int w) { return bar_done + 24u + 8u * w; };  // first half of P^T, dS^T written
+  auto bar_dpf = [&](int w) { return bar_done + 24u + 8u * w; };                // dP^T complete
+  auto bar_ptf = [&](int w) { return bar_done + 24u + 8u * (C::NSLOT + w); };  // P^T written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -250,9 +265,10 @@ __global__ void __maxnreg__(C::MAXREG)
     }
     for (int w = 0; w < C::NSLOT; ++w) {
       mbar_init(bar_sf(w), 1);
-      mbar_init(bar_pf(w), 4);  // one arrive per warp of the warpgroup
+      mbar_init(bar_dsf(w), 4);  // one arrive per warp of the warpgroup
       mbar_init(bar_gf(w), 1);
-      mbar_init(bar_ph(w), 4);
+      mbar_init(bar_dpf(w), 1);
+      mbar_init(bar_ptf(w), 4);
     }
     mbar_init(bar_done, 1);
     mbar_init(bar_drain, 1);
@@ -357,6 +373,7 @@ __global__ void __maxnreg__(C::MAXREG)
             const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
             mma_ss<0>(tmem + col, dk0 + oa, dqk0 + so + ob, idesc_s, kk > 0);
           }
+          mma_commit(bar_sf(s % C::NSLOT));  // S^T alone: the exponentials may start
 #pragma unroll
           for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
             const int e = kk * C::MMA_K;
@@ -364,14 +381,15 @@ __global__ void __maxnreg__(C::MAXREG)
             const uint32_t ob = ((e / C::CHUNK) * C::QS_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
             mma_ss<0>(tmem + col + C::BQ, dv0 + oa, ddok0 + so + ob, idesc_s, kk > 0);
           }
+          mma_commit(bar_dpf(s % C::NSLOT));
         }
         __syncwarp();
-        commit(bar_sf(s % C::NSLOT));
       }
       commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
     } else {
-      // dV += P^T dO and dK += dS^T Q of step s once its warpgroup has written P^T and dS^T.
+      // dV += P^T dO of step s as soon as its warpgroup has written P^T, dK += dS^T Q once it has written
+      // dS^T (the warpgroup forms dS^T while dV runs).
       constexpr uint32_t idesc_g = make_idesc(1, C::BK, C::D, 0, 1);   // B MN-major
       const uint64_t dqm0 = sdesc_sw128(sbase + C::OFF_Q, C::QS_CH_BYTES, 1024);   // Q as MN-major B
       const uint64_t ddom0 = sdesc_sw128(sbase + C::OFF_DO, C::QS_CH_BYTES, 1024); // dO as MN-major B
@@ -379,36 +397,31 @@ __global__ void __maxnreg__(C::MAXREG)
         const int st = s % C::STAGES;
         const uint32_t col = (s % C::NSLOT) * 2 * C::BQ;
         const uint64_t so = static_cast<uint64_t>((st * C::QS_BYTES) >> 4);
-        auto issue = [&](int kk0, int kk1) {
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = kk0; kk < kk1; ++kk) {
-              const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
-              mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
-                        (s > 0 || kk > 0) ? 1u : 0u);
-            }
-#pragma unroll
-            for (int kk = kk0; kk < kk1; ++kk) {
-              const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-              mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
-                        (s > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          __syncwarp();
-        };
         ok = wait_all(bar_full(st), (s / C::STAGES) & 1, WB_SF);  // complete already
-        // with HALF, the first half of the query rows as soon as the warpgroup has written it
-        constexpr int KH = C::HALF ? C::BQ / C::MMA_K / 2 : 0;
-        if (C::HALF) {
-          ok = ok && wait_all(bar_ph(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
-          if (!ok) break;
-          tc_fence_after();
-          issue(0, KH);
-        }
-        ok = ok && wait_all(bar_pf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
+        ok = ok && wait_all(bar_ptf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
         if (!ok) break;
         tc_fence_after();
-        issue(KH, C::BQ / C::MMA_K);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+            const uint32_t ob = (kk * C::MMA_K * 128) >> 4;  // 16 query rows = two 8-row swizzle atoms
+            mma_ts<0>(tmem + C::COL_DV, tmem + col + kk * (C::MMA_K / 2), ddom0 + so + ob, idesc_g,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+        ok = wait_all(bar_dsf(s % C::NSLOT), (s / C::NSLOT) & 1, WB_PF);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / C::MMA_K; ++kk) {
+            const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+            mma_ts<0>(tmem + C::COL_DK, tmem + col + C::BQ + kk * (C::MMA_K / 2), dqm0 + so + ob, idesc_g,
+                      (s > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        __syncwarp();
         commit(bar_gf(s % C::NSLOT));       // the slot may be overwritten
         commit(bar_empty(s % C::STAGES));   // the stage may be refilled (its score MMAs completed earlier)
       }
@@ -439,14 +452,24 @@ __global__ void __maxnreg__(C::MAXREG)
       const float4* rv = reinterpret_cast<const float4*>(smem + C::OFF_VEC + st * C::VEC_BYTES);
       // causal: query column q (row step_qt(s)*BQ + q) is visible to this key when q >= qmin
       const int qmin = p.causal ? key - p.causal_off - step_qt(s) * C::BQ : 0;
+      uint64_t pp[C::BQ / 2];
       if (__any_sync(0xffffffffu, qmin > 0))
-        dkdv_elementwise<C, true>(tS, tdP, rv, c2, qmin, bar_ph(w), lane);
+        dkdv_p_first<C, true>(tS, rv, c2, qmin, pp);
       else
-        dkdv_elementwise<C, false>(tS, tdP, rv, c2, qmin, bar_ph(w), lane);
+        dkdv_p_first<C, false>(tS, rv, c2, qmin, pp);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pf(w));
+      if (lane == 0) mbar_arrive(bar_ptf(w));  // dV += P^T dO may start
+      okw = mbar_wait(bar_dpf(w), (s / C::NSLOT) & 1, abort_flag, p.err, WB_SF);
+      ok = __all_sync(0xffffffffu, okw);
+      if (!ok) break;
+      tc_fence_after();
+      dkdv_ds_second<C>(tdP, rv, pp);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dsf(w));
     }
     // ---------------------------------------------------------- epilogue: warpgroup 0 writes dV, 1 writes dK
     bool okd = ok && w < 2 && mbar_wait(bar_done, 0, abort_flag, p.err, WB_DONE);
@@ -491,14 +514,13 @@ __global__ void __maxnreg__(C::MAXREG)
 
 // ------------------------------------------------------------------------------------------ dQ
 
-template <int D_, int BC_, int STAGES_, bool HALF_ = true, bool ATMEM_ = false>
+template <int D_, int BC_, int STAGES_, bool ATMEM_>
 struct BwdQCfg {
   static constexpr int D = D_;
   static constexpr int BR = 128;           // query rows per tile (TMEM lanes)
   static constexpr int NQT = 2;            // query tiles per CTA, alternating between the two warpgroups
   static constexpr int BC = BC_;           // keys per step
   static constexpr int STAGES = STAGES_;   // ring of (K_j, V_j)
-  static constexpr bool HALF = HALF_;      // dQ MMAs start on the first half of a step's keys
   // ATMEM: the elementwise warpgroups copy Q_t and dO_t into tensor memory once, and S and dP take
   // them as the A operand there: each MMA then reads only K or V from shared memory (an N = 64 MMA
   // reading both operands from shared memory is bound by its bandwidth).
@@ -515,13 +537,14 @@ struct BwdQCfg {
   static constexpr int OFF_K = OFF_DO + NQT * Q_BYTES;         // stage s at + s * KV_BYTES
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], p_full[NQT], o_done[NQT],
-  // g_free[NQT], drain (score issuer), drain (dQ issuer), p_half[NQT], a_in_tmem[NQT]
+  // barriers: q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NQT], ds_full[NQT],
+  // o_done[NQT], drain (S issuer), drain (dP, dQ issuer), a_in_tmem[NQT], s_read[NQT] (the warpgroup has
+  // read S), dp_full[NQT]
   static constexpr int NBAR = 1 + 4 * STAGES + 6 * NQT + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM: tile t holds S at t*2*BC and dP at t*2*BC + BC (dS, bf16 pairs, over the first BC/2 columns
-  // of S), dQ at 2*NQT*BC + t*D; with ATMEM, Q_t and dO_t as bf16 pairs (D/2 columns each) after them.
+  // of dP), dQ at 2*NQT*BC + t*D; with ATMEM, Q_t and dO_t as bf16 pairs (D/2 columns each) after them.
   static constexpr int COL_DQ = 2 * NQT * BC;
   static constexpr int COL_QA = COL_DQ + NQT * D;
   static constexpr int COL_DOA = COL_QA + NQT * (D / 2);
@@ -530,8 +553,8 @@ struct BwdQCfg {
   static constexpr int NWARPS = 4 * NQT + 3;
   static constexpr int NTHREADS = NWARPS * 32;
   static constexpr int LOAD_WARP = 4 * NQT;
-  static constexpr int MMA_WARP = 4 * NQT + 1;   // S, dP (two issuing warps, as in the dK/dV kernel)
-  static constexpr int GRAD_WARP = 4 * NQT + 2;  // dQ
+  static constexpr int MMA_WARP = 4 * NQT + 1;   // S (two issuing warps, as in the dK/dV kernel)
+  static constexpr int GRAD_WARP = 4 * NQT + 2;  // dQ, then the next step's dP
   static constexpr int MAXREG = RegBudget<NWARPS, 1>::VALUE;
   static_assert(D % CHUNK == 0 && BC % 64 == 0 && BC <= 128, "tile");
   static_assert(!ATMEM || NCH == 1, "A operands copied into tensor memory from one 128-byte row segment");
@@ -549,33 +572,25 @@ struct BwdQParams {
   float c, scale;
 };
 
-// One step of a dQ elementwise thread (one query row, BC key columns): P = 2^(s c - L log2 e),
-// dS = P (dP - D), written back over S as bf16 pairs.  TAIL: columns >= valid are masked (P = 0).
+// First part of a dQ elementwise step (thread = query row, BC key columns): P = 2^(s c - L log2 e) from S
+// into registers as f32 pairs.  TAIL: columns >= valid are masked (P = 0).  Every TMEM load has completed
+// on return, so the S issuer may overwrite S with the next step's.
 template <class C, bool TAIL>
-__device__ __forceinline__ void dq_elementwise(uint32_t tS, uint32_t tdP, uint64_t c2, uint64_t nl_2, uint64_t nd_2,
-                                               int valid, uint32_t bar_half, int lane) {
-  // 16-column chunks with the next chunk's TMEM loads in flight, as in the dK/dV kernel; chunk cc's
-  // 8 packed dS columns go over S columns 8 cc .. 8 cc + 7, all read already.
+__device__ __forceinline__ void dq_p_regs(uint32_t tS, uint64_t c2, uint64_t nl_2, int valid,
+                                          uint64_t (&pp)[C::BC / 2]) {
   constexpr int NCHK = C::BC / 16;
-  uint32_t sr[2][16], dr[2][16];
-  tmem_ld16(tS, sr[0]);
-  tmem_ld16(tdP, dr[0]);
-  tmem_wait_ld();
-  reg_fence(sr[0]);
-  reg_fence(dr[0]);
+  uint32_t sr[NCHK][16];
 #pragma unroll
-  for (int cc = 0; cc < NCHK; ++cc) {
-    if (cc + 1 < NCHK) {
-      tmem_ld16(tS + (cc + 1) * 16, sr[(cc + 1) & 1]);
-      tmem_ld16(tdP + (cc + 1) * 16, dr[(cc + 1) & 1]);
-    }
-    const uint32_t(&s16)[16] = sr[cc & 1];
-    const uint32_t(&d16)[16] = dr[cc & 1];
-    uint32_t pk[8];
+  for (int cc = 0; cc < NCHK; ++cc) tmem_ld16(tS + cc * 16, sr[cc]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int cc = 0; cc < NCHK; ++cc) reg_fence(sr[cc]);
+#pragma unroll
+  for (int cc = 0; cc < NCHK; ++cc)
 #pragma unroll
     for (int e = 0; e < 16; e += 2) {
       const int col = cc * 16 + e;
-      const uint64_t x = f2_fma(f2_pack(__uint_as_float(s16[e]), __uint_as_float(s16[e + 1])), c2, nl_2);
+      const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[cc][e]), __uint_as_float(sr[cc][e + 1])), c2, nl_2);
       float x0, x1;
       f2_unpack_f(x, x0, x1);
       float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -583,22 +598,36 @@ __device__ __forceinline__ void dq_elementwise(uint32_t tS, uint32_t tdP, uint64
         if (col >= valid) p0 = 0.f;
         if (col + 1 >= valid) p1 = 0.f;
       }
+      pp[col / 2] = f2_pack(p0, p1);
+    }
+}
+
+// Second part: dS = P (dP - D), written as bf16 pairs over the first BC/2 columns of dP, the A operand of
+// dQ += dS K (16-column chunks with the next chunk's TMEM load in flight; chunk cc's 8 packed columns go
+// over dP columns 8 cc .. 8 cc + 7, all read already).
+template <class C>
+__device__ __forceinline__ void dq_ds_regs(uint32_t tdP, uint64_t nd_2, const uint64_t (&pp)[C::BC / 2]) {
+  constexpr int NCHK = C::BC / 16;
+  uint32_t dr[2][16];
+  tmem_ld16(tdP, dr[0]);
+  tmem_wait_ld();
+  reg_fence(dr[0]);
+#pragma unroll
+  for (int cc = 0; cc < NCHK; ++cc) {
+    if (cc + 1 < NCHK) tmem_ld16(tdP + (cc + 1) * 16, dr[(cc + 1) & 1]);
+    const uint32_t(&d16)[16] = dr[cc & 1];
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
       const uint64_t tt = f2_add(f2_pack(__uint_as_float(d16[e]), __uint_as_float(d16[e + 1])), nd_2);
-      const uint64_t ds = f2_mul(f2_pack(p0, p1), tt);
+      const uint64_t ds = f2_mul(pp[(cc * 16 + e) / 2], tt);
       float ds0, ds1;
       f2_unpack_f(ds, ds0, ds1);
       pk[e / 2] = pack_bf16x2(ds0, ds1);
     }
-    tmem_st8(tS + cc * 8, pk);
-    if (C::HALF && cc == NCHK / 2 - 1) {  // the first half of the step's keys is in: dQ += dS K may start
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_half);
-    }
+    tmem_st8(tdP + cc * 8, pk);
     if (cc + 1 < NCHK) {
       tmem_wait_ld();
-      reg_fence(sr[(cc + 1) & 1]);
       reg_fence(dr[(cc + 1) & 1]);
     }
   }
@@ -635,11 +664,11 @@ __global__ void __maxnreg__(C::MAXREG)
   auto bar_sf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + t); };
   auto bar_pf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + C::NQT + t); };
   auto bar_od = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 2 * C::NQT + t); };
-  auto bar_gf = [&](int t) { return bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT + t); };
-  const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 4 * C::NQT);
+  const uint32_t bar_drain = bar0 + 8u * (1 + 4 * C::STAGES + 3 * C::NQT);
   const uint32_t bar_drain_g = bar_drain + 8u;
-  auto bar_ph = [&](int t) { return bar_drain + 16u + 8u * t; };  // first half of dS written
-  auto bar_qa = [&](int t) { return bar_drain + 16u + 8u * (C::NQT + t); };  // Q_t, dO_t in TMEM (ATMEM)
+  auto bar_qa = [&](int t) { return bar_drain + 16u + 8u * t; };                 // Q_t, dO_t in TMEM (ATMEM)
+  auto bar_sr = [&](int t) { return bar_drain + 16u + 8u * (C::NQT + t); };      // S_t read
+  auto bar_dpf = [&](int t) { return bar_drain + 16u + 8u * (2 * C::NQT + t); };  // dP_t complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -655,9 +684,9 @@ __global__ void __maxnreg__(C::MAXREG)
       mbar_init(bar_sf(t), 1);
       mbar_init(bar_pf(t), 4);
       mbar_init(bar_od(t), 1);
-      mbar_init(bar_gf(t), 1);
-      mbar_init(bar_ph(t), 4);
       mbar_init(bar_qa(t), 4);
+      mbar_init(bar_sr(t), 4);
+      mbar_init(bar_dpf(t), 1);
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain_g, 1);
@@ -729,98 +758,126 @@ __global__ void __maxnreg__(C::MAXREG)
       if (elect_one()) mma_commit(bar);
       __syncwarp();
     };
+    // S_t(j) = Q_t K_j^T and dP_t(j) = dO_t V_j^T (stage s), issued by the elected lane of the caller
+    constexpr uint32_t idesc_s = make_idesc(1, C::BR, C::BC, 0, 0);
+    const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+    const uint64_t ddo0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+    const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+    const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+    auto issue_s = [&](int t, int s) {
+      const uint32_t col = t * 2 * C::BC;
+      const uint64_t to = static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
+      const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+        const int e = kk * C::MMA_K;
+        const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        if constexpr (C::ATMEM)
+          mma_ts<0>(tmem + col, tmem + C::COL_QA + t * (C::D / 2) + kk * (C::MMA_K / 2), dk0 + so + ob, idesc_s,
+                    kk > 0);
+        else
+          mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
+      }
+    };
+    auto issue_dp = [&](int t, int s) {
+      const uint32_t col = t * 2 * C::BC + C::BC;
+      const uint64_t to = static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
+      const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
+        const int e = kk * C::MMA_K;
+        const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
+        if constexpr (C::ATMEM)
+          mma_ts<0>(tmem + col, tmem + C::COL_DOA + t * (C::D / 2) + kk * (C::MMA_K / 2), dv0 + so + ob, idesc_s,
+                    kk > 0);
+        else
+          mma_ss<0>(tmem + col, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
+      }
+    };
+    // dQ_t += dS_t K_j, dS_t read from tensor memory
+    constexpr uint32_t idesc_g = make_idesc(1, C::BR, C::D, 0, 1);  // K MN-major
+    const uint64_t dkm0 = sdesc_sw128(sbase + C::OFF_K, C::KV_CH_BYTES, 1024);
+    auto issue_dq = [&](int t, int s, int j) {
+      const uint32_t a_tmem = tmem + t * 2 * C::BC + C::BC;  // dS over dP
+      const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < C::BC / C::MMA_K; ++kk) {
+        const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
+        mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+      }
+    };
     if (warp == C::MMA_WARP) {
-      // S_t = Q_t K_j^T and dP_t = dO_t V_j^T once K_j, V_j have landed and dQ_t(j-1) -- the last reader
-      // of dS_t, which sits over S_t -- has completed.
-      constexpr uint32_t idesc_s = make_idesc(1, C::BR, C::BC, 0, 0);
-      const uint64_t dq0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-      const uint64_t ddo0 = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
-      const uint64_t dk0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-      const uint64_t dv0 = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
       bool ok = wait_all(bar_q, 0, WB_Q);
       if constexpr (C::ATMEM) {
 #pragma unroll
         for (int t = 0; t < C::NQT; ++t) ok = ok && wait_all(bar_qa(t), 0, WB_Q);
       }
+      // S_t(j) once K_j has landed and the warpgroup has read S_t(j-1) (it keeps P in registers)
       for (int j = 0; ok && j < T; ++j) {
         const int s = j % C::STAGES;
-        ok = wait_all(bar_kf(s), (j / C::STAGES) & 1, WB_KF) && wait_all(bar_vf(s), (j / C::STAGES) & 1, WB_VF);
+        ok = wait_all(bar_kf(s), (j / C::STAGES) & 1, WB_KF);
         for (int t = 0; ok && t < C::NQT; ++t) {
-          if (j > 0) ok = wait_all(bar_gf(t), (j - 1) & 1, WB_PF);
+          if (j > 0) ok = wait_all(bar_sr(t), (j - 1) & 1, WB_SE);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t col = t * 2 * C::BC;
-          const uint64_t to = static_cast<uint64_t>((t * C::Q_BYTES) >> 4);
-          const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
-          if (elect_one()) {  // one lane issues the whole batch
-#pragma unroll
-            for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-              const int e = kk * C::MMA_K;
-              const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-              const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-              if constexpr (C::ATMEM)
-                mma_ts<0>(tmem + col, tmem + C::COL_QA + t * (C::D / 2) + kk * (C::MMA_K / 2), dk0 + so + ob,
-                          idesc_s, kk > 0);
-              else
-                mma_ss<0>(tmem + col, dq0 + to + oa, dk0 + so + ob, idesc_s, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < C::D / C::MMA_K; ++kk) {
-              const int e = kk * C::MMA_K;
-              const uint32_t oa = ((e / C::CHUNK) * C::Q_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-              const uint32_t ob = ((e / C::CHUNK) * C::KV_CH_BYTES + (e % C::CHUNK) * 2) >> 4;
-              if constexpr (C::ATMEM)
-                mma_ts<0>(tmem + col + C::BC, tmem + C::COL_DOA + t * (C::D / 2) + kk * (C::MMA_K / 2),
-                          dv0 + so + ob, idesc_s, kk > 0);
-              else
-                mma_ss<0>(tmem + col + C::BC, ddo0 + to + oa, dv0 + so + ob, idesc_s, kk > 0);
-            }
-          }
+          if (elect_one()) issue_s(t, s);
           __syncwarp();
           commit(bar_sf(t));
         }
-        if (ok) commit(bar_ve(s));  // V_j is read by dP only
       }
       commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
     } else {
-      // dQ_t += dS_t K_j once the tile's warpgroup has written dS_t.
-      constexpr uint32_t idesc_g = make_idesc(1, C::BR, C::D, 0, 1);  // K MN-major
-      const uint64_t dkm0 = sdesc_sw128(sbase + C::OFF_K, C::KV_CH_BYTES, 1024);
-      bool ok = true;
+      // dQ_t(j) once the warpgroup has written dS_t(j) (over dP_t), then, from the same lane and so behind
+      // it in the tensor pipe (MMAs issued by one thread run in issue order), dP_t(j+1) into the columns
+      // dQ_t(j) reads.
+      bool ok = wait_all(bar_q, 0, WB_Q);
+      if constexpr (C::ATMEM) {
+#pragma unroll
+        for (int t = 0; t < C::NQT; ++t) ok = ok && wait_all(bar_qa(t), 0, WB_Q);
+      }
+      ok = ok && wait_all(bar_vf(0), 0, WB_VF);
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int t = 0; t < C::NQT; ++t) {
+            issue_dp(t, 0);
+            mma_commit(bar_dpf(t));
+          }
+          mma_commit(bar_ve(0));  // V_0 is read by dP only
+        }
+        __syncwarp();
+      }
       for (int j = 0; ok && j < T; ++j) {
         const int s = j % C::STAGES;
+        const bool nxt = j + 1 < T;
+        const int s1 = (j + 1) % C::STAGES;
         ok = wait_all(bar_kf(s), (j / C::STAGES) & 1, WB_KF);  // complete already: K_j was read by S
+        if (ok && nxt) ok = wait_all(bar_vf(s1), ((j + 1) / C::STAGES) & 1, WB_VF);
         for (int t = 0; ok && t < C::NQT; ++t) {
-          const uint32_t a_tmem = tmem + t * 2 * C::BC;
-          const uint64_t so = static_cast<uint64_t>((s * C::KV_BYTES) >> 4);
-          auto issue = [&](int kk0, int kk1) {
-            if (elect_one()) {
-#pragma unroll
-              for (int kk = kk0; kk < kk1; ++kk) {
-                const uint32_t ob = (kk * C::MMA_K * 128) >> 4;
-                mma_ts<0>(tmem + C::COL_DQ + t * C::D, a_tmem + kk * (C::MMA_K / 2), dkm0 + so + ob, idesc_g,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-              }
-            }
-            __syncwarp();
-          };
-          // with HALF, the first half of the keys as soon as the warpgroup has written their dS
-          constexpr int KH = C::HALF ? C::BC / C::MMA_K / 2 : 0;
-          if (C::HALF) {
-            ok = wait_all(bar_ph(t), j & 1, WB_PF);
-            if (!ok) break;
-            tc_fence_after();
-            issue(0, KH);
-          }
           ok = wait_all(bar_pf(t), j & 1, WB_PF);
           if (!ok) break;
           tc_fence_after();
-          issue(KH, C::BC / C::MMA_K);
-          commit(j + 1 < T ? bar_gf(t) : bar_od(t));
+          if (elect_one()) {
+            issue_dq(t, s, j);
+            if (nxt) {
+              issue_dp(t, s1);
+              mma_commit(bar_dpf(t));
+            } else {
+              mma_commit(bar_od(t));
+            }
+          }
+          __syncwarp();
         }
-        // K_j is read by S (complete before its dS existed) and by dQ, complete at this commit
-        if (ok) commit(bar_ke(s));
+        // K_j is read by S (complete before its dS existed) and by dQ; V_{j+1} by dP
+        if (ok) {
+          commit(bar_ke(s));
+          if (nxt) commit(bar_ve(s1));
+        }
       }
       commit(bar_drain_g);
       mbar_wait_drain(bar_drain_g, 0, p.err, WB_DRAIN);
@@ -875,10 +932,19 @@ __global__ void __maxnreg__(C::MAXREG)
       if (!ok) break;
       tc_fence_after();
       const int valid = row_lim - j * C::BC;  // key columns of this step the row may see
+      uint64_t pp[C::BC / 2];
       if (__all_sync(0xffffffffu, valid >= C::BC))
-        dq_elementwise<C, false>(tS, tdP, c2, nl_2, nd_2, valid, bar_ph(t), lane);
+        dq_p_regs<C, false>(tS, c2, nl_2, valid, pp);
       else
-        dq_elementwise<C, true>(tS, tdP, c2, nl_2, nd_2, valid, bar_ph(t), lane);
+        dq_p_regs<C, true>(tS, c2, nl_2, valid, pp);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sr(t));  // S_t may be overwritten by the next step's S
+      okw = mbar_wait(bar_dpf(t), j & 1, abort_flag, p.err, WB_SF);
+      ok = __all_sync(0xffffffffu, okw);
+      if (!ok) break;
+      tc_fence_after();
+      dq_ds_regs<C>(tdP, nd_2, pp);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
