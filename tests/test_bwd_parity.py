@@ -37,6 +37,7 @@ SHAPES = [
     (1, 1, 1, 64),       # one query row
     (1, 2, 300, 65),     # one key past a tile
     (1, 1, 513, 129),
+    (1, 3, 130, 17),     # fewer keys than one tile
 ]
 
 
@@ -49,6 +50,39 @@ def test_bwd_shapes(cuda_device, d, shape):
     dout = make_dout(B, H, Nq, d, "bf16", seed=1102 + Nq, device=cuda_device)
     sc, _, _, dq, dk, dv = _run(q, k, v, dout)
     check_bwd(q, k, v, dout, dq, dk, dv, sc, name=f"bwd d{d} {shape}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_single_key(cuda_device, dtype, d):
+    """One key: every P is 1, so dS = dP - D = 0 exactly, dQ = dK = 0 and dV_0 = sum_i dO_i.  The oracle
+    gives those exactly.  On the GPU, D comes from the stored O (V itself in bf16; V rounded to tf32,
+    relative error <= 2^-11, on the fp32 path) and dP from V, each summed in fp32 in its own order, so
+    |dS_i| <= eps * sum_c |dO_ic v_c| with eps = 4 d 2^-24 (+ 2^-11 for fp32), and
+    |dQ_ic| <= scale |dS_i| |k_c|, |dK_c| <= scale sum_i |dS_i| |q_ic| (twice that, for the roundings of
+    dS and of the stored gradients).  dV_0 = sum_i P_i dO_i with |P_i - 1| <= 16 u (1 + s_i) in bf16 and
+    another 2^-10 s_i on the fp32 path (the LSE comes from tf32 products), s_i = scale sum_c |q_ic k_c|,
+    plus the rounding of the stored dV (2^-9 relative in bf16)."""
+    B, H, Nq, Nk = 1, 3, 5, 1
+    q, k, v = make_qkv(B, H, Nq, Nk, d, dtype, seed=1480 + d, device=cuda_device)
+    dout = make_dout(B, H, Nq, d, dtype, seed=1481 + d, device=cuda_device)
+    sc = 1.0 / math.sqrt(d)
+    o, lse = fa.fa_fwd(q, k, v, scale=sc)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, dout, lse, scale=sc)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_error() == fa.FA_OK
+    qh, kh, vh, gh = (x.double().cpu() for x in (q, k, v, dout))
+    eps = 4 * d * 2.0 ** -24 + (2.0 ** -11 if dtype == "fp32" else 0.0)
+    ds_bound = eps * (gh.abs() * vh.abs()).sum(dim=-1, keepdim=True)  # [B, H, Nq, 1]
+    dq_bound = 2 * sc * ds_bound * kh.abs()                               # [B, H, Nq, d]
+    dk_bound = 2 * sc * (ds_bound * qh.abs()).sum(dim=2, keepdim=True)    # [B, H, 1, d]
+    assert (dq.double().cpu().abs() <= dq_bound + 1e-30).all()
+    assert (dk.double().cpu().abs() <= dk_bound + 1e-30).all()
+    s_abs = sc * (qh.abs() * kh.abs()).sum(dim=-1, keepdim=True)                    # [B, H, Nq, 1]
+    p_err = 16 * 2.0 ** -24 * (1 + s_abs) + (2.0 ** -10 * s_abs if dtype == "fp32" else 0.0)
+    ref_dv = gh.sum(dim=2, keepdim=True)
+    dv_bound = (p_err * gh.abs()).sum(dim=2, keepdim=True) + (2.0 ** -8 if dtype == "bf16" else 2.0 ** -22) * ref_dv.abs()
+    assert ((dv.double().cpu() - ref_dv).abs() <= dv_bound + 1e-30).all()
 
 
 @pytest.mark.parametrize("d", [64, 128])
