@@ -548,7 +548,9 @@ def measure_extras(fa, torch, accounting, dev, stream, launches=20, hbm_gbs=None
     `stream` after 3 warm-up launches (not part of `value`):
       causal        the two bf16 prefill workloads with the causal mask (visible-key FLOPs)
       gqa           B=4 H=16 N=4096 d=64 bf16 with 2 key/value heads
-      split_kv      B=1 H=1 N=4096 d=64 fp32 (TF32) with automatic key splits vs one split
+      split_kv      B=1 H=1 N=4096 d=64 fp32 (TF32) with automatic key splits vs one split (a call lasts
+                    tens of microseconds, less than its host-side submission: each call is timed alone
+                    behind an L2 flush, as the fp32 prefill entries are)
       decode_gqa    the decode workload (B=32, H=32 query heads, Nk=32768, d=64, 16 splits) with 8 and 4
                     key/value heads (groups of 4 and 8), GB/s of K/V read once plus q and o
       bwd           fa_bwd on the two bf16 prefill workloads, plain and causal, and on the fp32
@@ -568,6 +570,22 @@ def measure_extras(fa, torch, accounting, dev, stream, launches=20, hbm_gbs=None
         torch.cuda.synchronize()
         return a.elapsed_time(b) / launches
 
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed_each(fn, n=50):
+        # one call per event pair, each behind an L2 flush whose run covers the call's host-side submission
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                flush.fill_(1)
+                a.record(stream)
+                fn()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
     out = {}
     for name in PREFILL:
         w = WORKLOADS[name]
@@ -583,10 +601,12 @@ def measure_extras(fa, torch, accounting, dev, stream, launches=20, hbm_gbs=None
     w = WORKLOADS["long_fp32"]
     q, k, v = workload_inputs(w, device=dev)
     fl = accounting.fwd_flops(w.B, w.H, w.Nq, w.Nk, w.d)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), device=dev, dtype=torch.float32)
     for tag, ks in (("split_kv_auto", 0), ("split_kv_off", 1)):
-        ms = timed(lambda: fa.fa_fwd(q, k, v, scale=w.scale, kv_splits=ks, stream=stream))
-        out[f"{tag}_long_fp32"] = {"ms": ms, "tflops": fl / ms / 1e9}
-    del q, k, v
+        ms = timed_each(lambda: fa.fa_fwd(q, k, v, scale=w.scale, o=o, lse=lse, kv_splits=ks, stream=stream))
+        out[f"{tag}_long_fp32"] = {"ms": ms, "tflops": fl / ms / 1e9, "l2": "flushed before every timed call"}
+    del q, k, v, o, lse, flush
     w = WORKLOADS["decode"]
     qd, _, _ = make_qkv(w.B, w.H, 1, 1, w.d, "bf16", seed=w.seed, device=dev)
     for hkv in (8, 4):
