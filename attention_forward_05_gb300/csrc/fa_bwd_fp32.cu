@@ -21,8 +21,9 @@
 //                            and accumulates dQ of its rows in registers
 // Both main kernels are shared-memory tiled products: each of the 256 threads owns a 4 x 4 (d = 64)
 // or 4 x 2 (d = 128) block of the step's score tile and a 4 x (d/16) block of the accumulated
-// gradient tile.  Operands read along the reduction index are kept transposed in shared memory, with
-// rows padded to whole 16-byte groups, so that each thread reads its operands as vectors.
+// gradient tile.  Every operand stays row-major in shared memory (rows padded by 16 bytes, so the
+// 16-byte reads of a quarter-warp hit distinct banks), and the next step's tiles stream in with
+// asynchronous copies while the current step computes.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -65,47 +66,6 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_fp32_kernel(const float* __re
   }
 }
 
-// dst[c][r] = src[r][c] for the NROWS rows of a [*, D] fp32 block (rows >= valid read as zero); dst
-// has `ld` words per c.  Each thread loads all its elements before storing any, so the block's global
-// loads are in flight together.
-template <int D, int NROWS>
-__device__ __forceinline__ void load_transposed(float* dst, int ld, const float* src, int valid) {
-  constexpr int PER = NROWS * D / BW_THREADS;
-  static_assert(PER * BW_THREADS == NROWS * D, "whole rounds");
-  float x[PER];
-#pragma unroll
-  for (int it = 0; it < PER; ++it) {
-    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
-    const int r = idx / D, c = idx % D;
-    x[it] = r < valid ? src[static_cast<size_t>(r) * D + c] : 0.f;
-  }
-#pragma unroll
-  for (int it = 0; it < PER; ++it) {
-    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
-    dst[(idx % D) * ld + idx / D] = x[it];
-  }
-}
-
-// dst[r][c] = src[r][c] (row-major, D words per row) for the NROWS rows (rows >= valid read as zero).
-template <int D, int NROWS>
-__device__ __forceinline__ void load_rows(float* dst, const float* src, int valid) {
-  constexpr int PER = NROWS * D / 4 / BW_THREADS;
-  static_assert(PER * BW_THREADS * 4 == NROWS * D, "whole rounds");
-  float4 x[PER];
-#pragma unroll
-  for (int it = 0; it < PER; ++it) {
-    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
-    const int r = idx / (D / 4), c4 = idx % (D / 4);
-    x[it] = r < valid ? reinterpret_cast<const float4*>(src + static_cast<size_t>(r) * D)[c4]
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int it = 0; it < PER; ++it) {
-    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
-    reinterpret_cast<float4*>(dst + (idx / (D / 4)) * D)[idx % (D / 4)] = x[it];
-  }
-}
-
 struct BwdF32Params {
   const float *q, *k, *v, *dout, *nl, *negd;
   float *dq, *dk, *dv;
@@ -115,59 +75,84 @@ struct BwdF32Params {
 
 // Tile shapes.  A CTA owns BM = 64 rows (keys in the dK/dV kernel, query rows in the dQ kernel) and
 // streams BN rows of the other side per step: 64 at d = 64, 32 at d = 128 (shared memory).  Thread
-// (ty, tx) of 16 x 16 owns rows 4 ty .. 4 ty + 3 of the CTA's side, and in the step's score tile the
-// TQ = BN / 16 columns TQ tx ..; in the accumulated gradient tile the CW = d / 16 columns CW tx ...
-// Arrays read along the reduction index are transposed, with rows padded to a multiple of 4 floats
-// so that every read is one 16-byte (or 8-byte) load.
+// (ty, tx) of 16 x 16 owns the CTA-side rows ty + 16 r (r < 4), the step-side rows tx + 16 q (q < TQ)
+// of the step's score tile, and the gradient columns 64 h + 4 tx .. + 3 (h < d / 64).  Every operand
+// sits row-major in shared memory with rows padded to D + 4 floats, so that the 16-byte reads of a
+// quarter-warp (eight consecutive step-side rows, or one row's consecutive columns) hit distinct
+// banks, and a CTA-side read is a broadcast.  P^T / dS (written by the score phase, read by the
+// gradient phase) are stored by step-side row with the thread's four CTA-side rows adjacent: column
+// 4 ty + r holds CTA row ty + 16 r.
 template <int D>
 struct F32Tile {
   static constexpr int BM = BW_M;
   static constexpr int BN = D == 64 ? 64 : 32;
   static constexpr int TQ = BN / 16;
-  static constexpr int CW = D / 16;
-  static constexpr int MP = BM + 4;  // padded row of a transposed BM-row block
-  static constexpr int NP = BN + 4;  // padded row of a transposed BN-row block
+  static constexpr int NH = D / 64;        // 4-column groups of gradient columns per thread
+  static constexpr int LD = D + 4;         // padded row of a [rows][D] tile
+  static constexpr int MP = BM + 4;        // padded row of a [step rows][BM] tile
 };
 
 template <int N>
 __device__ __forceinline__ void lds_vec(float (&r)[N], const float* p) {
-  static_assert(N == 2 || N == 4, "vector width");
-  if constexpr (N == 4) {
-    const float4 x = *reinterpret_cast<const float4*>(p);
-    r[0] = x.x;
-    r[1] = x.y;
-    r[2] = x.z;
-    r[3] = x.w;
-  } else {
-    const float2 x = *reinterpret_cast<const float2*>(p);
-    r[0] = x.x;
-    r[1] = x.y;
+  static_assert(N == 4, "vector width");
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  r[0] = x.x;
+  r[1] = x.y;
+  r[2] = x.z;
+  r[3] = x.w;
+}
+
+// 16-byte asynchronous copy global -> shared; `ok` false writes zeros (the source is not read).
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// dst[r][c] = src[r][c] for the NROWS rows of a [*, D] fp32 block into rows of LD floats (rows >= valid
+// are zero), as 16-byte asynchronous copies spread over the CTA's threads.  src is row 0 of the block,
+// always a valid row.
+template <int D, int NROWS>
+__device__ __forceinline__ void copy_rows_async(float* dst, const float* src, int valid) {
+  constexpr int G = D / 4;
+  constexpr int PER = NROWS * G / BW_THREADS;
+  static_assert(PER * BW_THREADS == NROWS * G, "whole rounds");
+#pragma unroll
+  for (int it = 0; it < PER; ++it) {
+    const int idx = it * BW_THREADS + static_cast<int>(threadIdx.x);
+    const int r = idx / G, g = idx % G;
+    const bool ok = r < valid;
+    cp_async16(dst + r * (D + 4) + 4 * g, src + static_cast<size_t>(ok ? r : 0) * D + 4 * g, ok);
   }
 }
 
-// Shared memory of the dK/dV kernel (floats): K^T, V^T [D][MP]; per step Q^T, dO^T [D][NP], Q, dO
-// [BN][D]; P^T and dS^T as [BN query rows][MP]; the step's nl and -D.
+// n floats (a multiple of 4, 16-byte aligned on both sides) by threads 0 .. n/4 - 1.
+__device__ __forceinline__ void copy_vec_async(float* dst, const float* src, int n) {
+  const int g = static_cast<int>(threadIdx.x);
+  if (g < n / 4) cp_async16(dst + 4 * g, src + 4 * g, true);
+}
+
+// Shared memory of the dK/dV kernel (floats): K, V [BM][LD]; two stages of Q, dO [BN][LD] and the step's
+// nl, -D [BN]; P^T and dS^T as [BN][MP].
 template <int D>
 constexpr int dkdv_smem_floats() {
   using T = F32Tile<D>;
-  return 2 * D * T::MP + 2 * D * T::NP + 2 * T::BN * D + 2 * T::BN * T::MP + 2 * T::BN;
+  return 2 * T::BM * T::LD + 2 * (2 * T::BN * T::LD + 2 * T::BN) + 2 * T::BN * T::MP;
 }
 
 template <int D>
 __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF32Params p) {
   using T = F32Tile<D>;
-  constexpr int BM = T::BM, BN = T::BN, TQ = T::TQ, CW = T::CW, MP = T::MP, NP = T::NP;
+  constexpr int BM = T::BM, BN = T::BN, TQ = T::TQ, NH = T::NH, LD = T::LD, MP = T::MP;
+  constexpr int STAGE = 2 * BN * LD + 2 * BN;
   extern __shared__ __align__(16) float sm[];
-  float* kt = sm;                       // [D][MP]
-  float* vt = kt + D * MP;              // [D][MP]
-  float* qt = vt + D * MP;              // [D][NP]
-  float* dot = qt + D * NP;             // [D][NP]
-  float* qr = dot + D * NP;             // [BN][D]
-  float* dor = qr + BN * D;             // [BN][D]
-  float* ps = dor + BN * D;             // [BN][MP]: P^T of the step, by query row
+  float* ks = sm;                       // [BM][LD]
+  float* vs = ks + BM * LD;             // [BM][LD]
+  float* st0 = vs + BM * LD;            // stage s at st0 + s * STAGE: Q [BN][LD], dO [BN][LD], nl [BN], -D [BN]
+  float* ps = st0 + 2 * STAGE;          // [BN][MP]: P^T of the step, by query row
   float* dss = ps + BN * MP;            // [BN][MP]: dS^T of the step
-  float* nl_s = dss + BN * MP;          // [BN]
-  float* nd_s = nl_s + BN;              // [BN]
 
   const int n_kblk = (p.Nk + BM - 1) / BM;
   const int kb = static_cast<int>(blockIdx.x % n_kblk);
@@ -176,145 +161,161 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dkdv_fp32_kernel(const BwdF
   const int G = p.H / p.Hkv;
   const int k0 = kb * BM;
   const int kvalid = min(BM, p.Nk - k0);
-  const float* kg = p.k + (static_cast<size_t>(bhkv) * p.Nk + k0) * D;
-  const float* vg = p.v + (static_cast<size_t>(bhkv) * p.Nk + k0) * D;
-  load_transposed<D, BM>(kt, MP, kg, kvalid);
-  load_transposed<D, BM>(vt, MP, vg, kvalid);
+  copy_rows_async<D, BM>(ks, p.k + (static_cast<size_t>(bhkv) * p.Nk + k0) * D, kvalid);
+  copy_rows_async<D, BM>(vs, p.v + (static_cast<size_t>(bhkv) * p.Nk + k0) * D, kvalid);
+  cp_async_commit();
   // The prep grid's row values are read below, after its completion.  Once every CTA of this grid has
   // passed that point the dQ grid, which reads the same values and nothing this grid writes, may start
   // on the SMs this grid leaves idle.
   griddep_wait();
   griddep_launch_dependents();
 
+  // steps: (query head g of the group, query tile i0), query tiles that see any key of this block
+  const int i_first = p.causal ? max(0, k0 - p.causal_off) : 0;
+  const int i_start = i_first / BN * BN;
+  const int n_i = (p.Nq - i_start + BN - 1) / BN;
+  const int n_steps = G * n_i;
+  auto step_bh = [&](int t) { return static_cast<size_t>(b) * p.H + hkv * G + t / n_i; };
+  auto step_i0 = [&](int t) { return i_start + (t % n_i) * BN; };
+  auto issue_step = [&](int t) {
+    float* st = st0 + (t & 1) * STAGE;
+    const size_t bh = step_bh(t);
+    const int i0 = step_i0(t);
+    const int qvalid = min(BN, p.Nq - i0);
+    copy_rows_async<D, BN>(st, p.q + (bh * p.Nq + i0) * D, qvalid);
+    copy_rows_async<D, BN>(st + BN * LD, p.dout + (bh * p.Nq + i0) * D, qvalid);
+    copy_vec_async(st + 2 * BN * LD, p.nl + bh * p.Nq_pad + i0, BN);  // Nq_pad >= every i0 + BN read here
+    copy_vec_async(st + 2 * BN * LD + BN, p.negd + bh * p.Nq_pad + i0, BN);
+    cp_async_commit();
+  };
+  issue_step(0);
+
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float dv_acc[4][CW], dk_acc[4][CW];
+  float dv_acc[4][4 * NH], dk_acc[4][4 * NH];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int c = 0; c < CW; ++c) dv_acc[r][c] = dk_acc[r][c] = 0.f;
+    for (int c = 0; c < 4 * NH; ++c) dv_acc[r][c] = dk_acc[r][c] = 0.f;
 
-  // query rows that see any key of this block: i >= k0 - causal_off under the mask
-  const int i_first = p.causal ? max(0, k0 - p.causal_off) : 0;
-  const int i_start = i_first / BN * BN;
-  for (int g = 0; g < G; ++g) {
-    const size_t bh = static_cast<size_t>(b) * p.H + hkv * G + g;
-    for (int i0 = i_start; i0 < p.Nq; i0 += BN) {
-      const int qvalid = min(BN, p.Nq - i0);
-      __syncthreads();  // the previous step's tiles are no longer read
-      const float* qg = p.q + (bh * p.Nq + i0) * D;
-      const float* dg = p.dout + (bh * p.Nq + i0) * D;
-      load_transposed<D, BN>(qt, NP, qg, qvalid);
-      load_transposed<D, BN>(dot, NP, dg, qvalid);
-      load_rows<D, BN>(qr, qg, qvalid);
-      load_rows<D, BN>(dor, dg, qvalid);
-      if (threadIdx.x < BN) {
-        const size_t rr = bh * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= every i0 + BN read here
-        nl_s[threadIdx.x] = p.nl[rr];
-        nd_s[threadIdx.x] = p.negd[rr];
+  for (int t = 0; t < n_steps; ++t) {
+    if (t + 1 < n_steps) {
+      issue_step(t + 1);  // into the other stage, released at the end of step t - 1
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // every thread's copies of step t (and of K, V) are in
+    const float* qs = st0 + (t & 1) * STAGE;
+    const float* dos = qs + BN * LD;
+    const float* nl_s = dos + BN * LD;
+    const float* nd_s = nl_s + BN;
+    const int i0 = step_i0(t);
+    // S^T = K Q^T and dP^T = V dO^T for this thread's 4 x TQ block, summed over c in order
+    float s[4][TQ], dp[4][TQ];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int qq = 0; qq < TQ; ++qq) s[r][qq] = dp[r][qq] = 0.f;
+#pragma unroll 2
+    for (int c = 0; c < D; c += 4) {
+      float a[4][4], av[4][4], bq[TQ][4], bg[TQ][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        lds_vec(a[r], ks + (ty + 16 * r) * LD + c);
+        lds_vec(av[r], vs + (ty + 16 * r) * LD + c);
       }
-      __syncthreads();
-      // S^T = K Q^T and dP^T = V dO^T for this thread's 4 x TQ block
-      float s[4][TQ], dp[4][TQ];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int qq = 0; qq < TQ; ++qq) {
+        lds_vec(bq[qq], qs + (tx + 16 * qq) * LD + c);
+        lds_vec(bg[qq], dos + (tx + 16 * qq) * LD + c);
+      }
 #pragma unroll
-        for (int qq = 0; qq < TQ; ++qq) s[r][qq] = dp[r][qq] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < D; ++c) {
-        float a[4], av[4], bq[TQ], bg[TQ];
-        lds_vec(a, kt + c * MP + 4 * ty);
-        lds_vec(av, vt + c * MP + 4 * ty);
-        lds_vec(bq, qt + c * NP + TQ * tx);
-        lds_vec(bg, dot + c * NP + TQ * tx);
+      for (int e = 0; e < 4; ++e)
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
           for (int qq = 0; qq < TQ; ++qq) {
-            s[r][qq] = fmaf(a[r], bq[qq], s[r][qq]);
-            dp[r][qq] = fmaf(av[r], bg[qq], dp[r][qq]);
+            s[r][qq] = fmaf(a[r][e], bq[qq][e], s[r][qq]);
+            dp[r][qq] = fmaf(av[r][e], bg[qq][e], dp[r][qq]);
           }
-      }
-      // P^T and dS^T; masked pairs (key past Nk or past the row's causal limit, row past Nq) give 0
+    }
+    // P^T and dS^T; masked pairs (key past Nk or past the row's causal limit, row past Nq) give 0
 #pragma unroll
-      for (int qq = 0; qq < TQ; ++qq) {
-        const int il = TQ * tx + qq, i = i0 + il;
-        const float nli = nl_s[il], ndi = nd_s[il];
-        float pr[4], dsr[4];
+    for (int qq = 0; qq < TQ; ++qq) {
+      const int il = tx + 16 * qq, i = i0 + il;
+      const float nli = nl_s[il], ndi = nd_s[il];
+      float pr[4], dsr[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int kj = k0 + 4 * ty + r;
-          const bool vis = kj < p.Nk && i < p.Nq && (!p.causal || kj <= i + p.causal_off);
-          pr[r] = vis ? ex2_approx(fmaf(s[r][qq], p.c, nli)) : 0.f;
-          dsr[r] = pr[r] * (dp[r][qq] + ndi);
-        }
-        *reinterpret_cast<float4*>(ps + il * MP + 4 * ty) = make_float4(pr[0], pr[1], pr[2], pr[3]);
-        *reinterpret_cast<float4*>(dss + il * MP + 4 * ty) = make_float4(dsr[0], dsr[1], dsr[2], dsr[3]);
+      for (int r = 0; r < 4; ++r) {
+        const int kj = k0 + ty + 16 * r;
+        const bool vis = kj < p.Nk && i < p.Nq && (!p.causal || kj <= i + p.causal_off);
+        pr[r] = vis ? ex2_approx(fmaf(s[r][qq], p.c, nli)) : 0.f;
+        dsr[r] = pr[r] * (dp[r][qq] + ndi);
       }
-      __syncthreads();
-      // dV += P^T dO, dK += dS^T Q over the step's query rows
+      *reinterpret_cast<float4*>(ps + il * MP + 4 * ty) = make_float4(pr[0], pr[1], pr[2], pr[3]);
+      *reinterpret_cast<float4*>(dss + il * MP + 4 * ty) = make_float4(dsr[0], dsr[1], dsr[2], dsr[3]);
+    }
+    __syncthreads();
+    // dV += P^T dO, dK += dS^T Q over the step's query rows, in order
 #pragma unroll 4
-      for (int il = 0; il < BN; ++il) {
-        float pr[4], dr[4], go[CW], qv[CW];
-        lds_vec(pr, ps + il * MP + 4 * ty);
-        lds_vec(dr, dss + il * MP + 4 * ty);
+    for (int il = 0; il < BN; ++il) {
+      float pr[4], dr[4], go[NH][4], qv[NH][4];
+      lds_vec(pr, ps + il * MP + 4 * ty);
+      lds_vec(dr, dss + il * MP + 4 * ty);
 #pragma unroll
-        for (int c4 = 0; c4 < CW; c4 += 4) {
-          float t0[4], t1[4];
-          lds_vec(t0, dor + il * D + tx * CW + c4);
-          lds_vec(t1, qr + il * D + tx * CW + c4);
+      for (int h = 0; h < NH; ++h) {
+        lds_vec(go[h], dos + il * LD + 64 * h + 4 * tx);
+        lds_vec(qv[h], qs + il * LD + 64 * h + 4 * tx);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            go[c4 + e] = t0[e];
-            qv[c4 + e] = t1[e];
+            dv_acc[r][4 * h + e] = fmaf(pr[r], go[h][e], dv_acc[r][4 * h + e]);
+            dk_acc[r][4 * h + e] = fmaf(dr[r], qv[h][e], dk_acc[r][4 * h + e]);
           }
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int c = 0; c < CW; ++c) {
-            dv_acc[r][c] = fmaf(pr[r], go[c], dv_acc[r][c]);
-            dk_acc[r][c] = fmaf(dr[r], qv[c], dk_acc[r][c]);
-          }
-      }
     }
+    __syncthreads();  // this stage and P^T, dS^T may be overwritten
   }
+  cp_async_wait<0>();  // n_steps >= 1, so every copy was waited for above; kept for a zero-step grid
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    const int kl = 4 * ty + r;
+    const int kl = ty + 16 * r;
     if (kl >= kvalid) continue;
-    const size_t off = (static_cast<size_t>(bhkv) * p.Nk + k0 + kl) * D + tx * CW;
+    const size_t off = (static_cast<size_t>(bhkv) * p.Nk + k0 + kl) * D + 4 * tx;
 #pragma unroll
-    for (int c4 = 0; c4 < CW; c4 += 4) {
-      *reinterpret_cast<float4*>(p.dv + off + c4) =
-          make_float4(dv_acc[r][c4], dv_acc[r][c4 + 1], dv_acc[r][c4 + 2], dv_acc[r][c4 + 3]);
-      *reinterpret_cast<float4*>(p.dk + off + c4) =
-          make_float4(dk_acc[r][c4] * p.scale, dk_acc[r][c4 + 1] * p.scale, dk_acc[r][c4 + 2] * p.scale,
-                      dk_acc[r][c4 + 3] * p.scale);
+    for (int h = 0; h < NH; ++h) {
+      *reinterpret_cast<float4*>(p.dv + off + 64 * h) =
+          make_float4(dv_acc[r][4 * h], dv_acc[r][4 * h + 1], dv_acc[r][4 * h + 2], dv_acc[r][4 * h + 3]);
+      *reinterpret_cast<float4*>(p.dk + off + 64 * h) =
+          make_float4(dk_acc[r][4 * h] * p.scale, dk_acc[r][4 * h + 1] * p.scale, dk_acc[r][4 * h + 2] * p.scale,
+                      dk_acc[r][4 * h + 3] * p.scale);
     }
   }
 }
 
-// Shared memory of the dQ kernel (floats): Q^T, dO^T [D][MP]; per step K^T, V^T [D][NP], K [BN][D];
-// dS as [BN keys][MP]; the CTA's nl and -D.
+// Shared memory of the dQ kernel (floats): Q, dO [BM][LD] and the CTA's nl, -D [BM]; two stages of K, V
+// [BN][LD]; dS as [BN keys][MP].
 template <int D>
 constexpr int dq_smem_floats() {
   using T = F32Tile<D>;
-  return 2 * D * T::MP + 2 * D * T::NP + T::BN * D + T::BN * T::MP + 2 * T::BM;
+  return 2 * T::BM * T::LD + 2 * T::BM + 2 * (2 * T::BN * T::LD) + T::BN * T::MP;
 }
 
 template <int D>
 __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32Params p) {
   using T = F32Tile<D>;
-  constexpr int BM = T::BM, BN = T::BN, TQ = T::TQ, CW = T::CW, MP = T::MP, NP = T::NP;
+  constexpr int BM = T::BM, BN = T::BN, TQ = T::TQ, NH = T::NH, LD = T::LD, MP = T::MP;
+  constexpr int STAGE = 2 * BN * LD;
   extern __shared__ __align__(16) float sm[];
-  float* qt = sm;                       // [D][MP]
-  float* dot = qt + D * MP;             // [D][MP]
-  float* kt = dot + D * MP;             // [D][NP]
-  float* vt = kt + D * NP;              // [D][NP]
-  float* kr = vt + D * NP;              // [BN][D]
-  float* dss = kr + BN * D;             // [BN keys][MP]
-  float* nl_s = dss + BN * MP;          // [BM]
+  float* qs = sm;                       // [BM][LD]
+  float* dos = qs + BM * LD;            // [BM][LD]
+  float* nl_s = dos + BM * LD;          // [BM]
   float* nd_s = nl_s + BM;              // [BM]
+  float* st0 = nd_s + BM;               // stage s at st0 + s * STAGE: K [BN][LD], V [BN][LD]
+  float* dss = st0 + 2 * STAGE;         // [BN keys][MP]
 
   const int n_qblk = (p.Nq + BM - 1) / BM;
   const int qb = static_cast<int>(blockIdx.x % n_qblk);
@@ -323,62 +324,79 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32
   const int bhkv = b * p.Hkv + h / (p.H / p.Hkv);
   const int i0 = qb * BM;
   const int qvalid = min(BM, p.Nq - i0);
-  const float* qg = p.q + (static_cast<size_t>(bh) * p.Nq + i0) * D;
-  const float* dg = p.dout + (static_cast<size_t>(bh) * p.Nq + i0) * D;
-  load_transposed<D, BM>(qt, MP, qg, qvalid);
-  load_transposed<D, BM>(dot, MP, dg, qvalid);
-  if (threadIdx.x < BM) {
-    const size_t rr = static_cast<size_t>(bh) * p.Nq_pad + i0 + threadIdx.x;  // Nq_pad >= i0 + BM
-    nl_s[threadIdx.x] = p.nl[rr];
-    nd_s[threadIdx.x] = p.negd[rr];
-  }
-
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float dq_acc[4][CW];
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int c = 0; c < CW; ++c) dq_acc[r][c] = 0.f;
+  copy_rows_async<D, BM>(qs, p.q + (static_cast<size_t>(bh) * p.Nq + i0) * D, qvalid);
+  copy_rows_async<D, BM>(dos, p.dout + (static_cast<size_t>(bh) * p.Nq + i0) * D, qvalid);
+  copy_vec_async(nl_s, p.nl + static_cast<size_t>(bh) * p.Nq_pad + i0, BM);  // Nq_pad >= i0 + BM
+  copy_vec_async(nd_s, p.negd + static_cast<size_t>(bh) * p.Nq_pad + i0, BM);
+  cp_async_commit();
 
   // keys any row of this block sees: j <= i0 + BM - 1 + causal_off under the mask
   const int k_end = p.causal ? min(p.Nk, i0 + BM + p.causal_off) : p.Nk;
-  for (int j0 = 0; j0 < k_end; j0 += BN) {
+  const int n_steps = (k_end + BN - 1) / BN;
+  auto issue_step = [&](int t) {
+    float* st = st0 + (t & 1) * STAGE;
+    const int j0 = t * BN;
     const int kvalid = min(BN, p.Nk - j0);
-    __syncthreads();  // the previous step's tiles are no longer read (and the CTA's tiles are in)
-    const float* kg = p.k + (static_cast<size_t>(bhkv) * p.Nk + j0) * D;
-    const float* vg = p.v + (static_cast<size_t>(bhkv) * p.Nk + j0) * D;
-    load_transposed<D, BN>(kt, NP, kg, kvalid);
-    load_transposed<D, BN>(vt, NP, vg, kvalid);
-    load_rows<D, BN>(kr, kg, kvalid);
+    copy_rows_async<D, BN>(st, p.k + (static_cast<size_t>(bhkv) * p.Nk + j0) * D, kvalid);
+    copy_rows_async<D, BN>(st + BN * LD, p.v + (static_cast<size_t>(bhkv) * p.Nk + j0) * D, kvalid);
+    cp_async_commit();
+  };
+  issue_step(0);
+
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float dq_acc[4][4 * NH];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4 * NH; ++c) dq_acc[r][c] = 0.f;
+
+  for (int t = 0; t < n_steps; ++t) {
+    if (t + 1 < n_steps) {
+      issue_step(t + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
     __syncthreads();
-    // S = Q K^T and dP = dO V^T for this thread's 4 x TQ block
+    const float* kst = st0 + (t & 1) * STAGE;
+    const float* vst = kst + BN * LD;
+    const int j0 = t * BN;
+    // S = Q K^T and dP = dO V^T for this thread's 4 x TQ block, summed over c in order
     float s[4][TQ], dp[4][TQ];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int kk = 0; kk < TQ; ++kk) s[r][kk] = dp[r][kk] = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < D; ++c) {
-      float a[4], ag[4], bk[TQ], bv[TQ];
-      lds_vec(a, qt + c * MP + 4 * ty);
-      lds_vec(ag, dot + c * MP + 4 * ty);
-      lds_vec(bk, kt + c * NP + TQ * tx);
-      lds_vec(bv, vt + c * NP + TQ * tx);
+#pragma unroll 2
+    for (int c = 0; c < D; c += 4) {
+      float a[4][4], ag[4][4], bk[TQ][4], bv[TQ][4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 4; ++r) {
+        lds_vec(a[r], qs + (ty + 16 * r) * LD + c);
+        lds_vec(ag[r], dos + (ty + 16 * r) * LD + c);
+      }
 #pragma unroll
-        for (int kk = 0; kk < TQ; ++kk) {
-          s[r][kk] = fmaf(a[r], bk[kk], s[r][kk]);
-          dp[r][kk] = fmaf(ag[r], bv[kk], dp[r][kk]);
-        }
+      for (int kk = 0; kk < TQ; ++kk) {
+        lds_vec(bk[kk], kst + (tx + 16 * kk) * LD + c);
+        lds_vec(bv[kk], vst + (tx + 16 * kk) * LD + c);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int kk = 0; kk < TQ; ++kk) {
+            s[r][kk] = fmaf(a[r][e], bk[kk][e], s[r][kk]);
+            dp[r][kk] = fmaf(ag[r][e], bv[kk][e], dp[r][kk]);
+          }
     }
 #pragma unroll
     for (int kk = 0; kk < TQ; ++kk) {
-      const int jl = TQ * tx + kk, j = j0 + jl;
+      const int jl = tx + 16 * kk, j = j0 + jl;
       float dsr[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int il = 4 * ty + r, i = i0 + il;
+        const int il = ty + 16 * r, i = i0 + il;
         const bool vis = j < p.Nk && i < p.Nq && (!p.causal || j <= i + p.causal_off);
         const float pr = vis ? ex2_approx(fmaf(s[r][kk], p.c, nl_s[il])) : 0.f;
         dsr[r] = pr * (dp[r][kk] + nd_s[il]);
@@ -386,34 +404,33 @@ __global__ void __launch_bounds__(BW_THREADS) fa_bwd_dq_fp32_kernel(const BwdF32
       *reinterpret_cast<float4*>(dss + jl * MP + 4 * ty) = make_float4(dsr[0], dsr[1], dsr[2], dsr[3]);
     }
     __syncthreads();
-    // dQ += dS K over the step's keys
+    // dQ += dS K over the step's keys, in order
 #pragma unroll 4
     for (int jl = 0; jl < BN; ++jl) {
-      float dr[4], kv[CW];
+      float dr[4], kv[NH][4];
       lds_vec(dr, dss + jl * MP + 4 * ty);
 #pragma unroll
-      for (int c4 = 0; c4 < CW; c4 += 4) {
-        float t0[4];
-        lds_vec(t0, kr + jl * D + tx * CW + c4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) kv[c4 + e] = t0[e];
-      }
+      for (int hh = 0; hh < NH; ++hh) lds_vec(kv[hh], kst + jl * LD + 64 * hh + 4 * tx);
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int c = 0; c < CW; ++c) dq_acc[r][c] = fmaf(dr[r], kv[c], dq_acc[r][c]);
+        for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dq_acc[r][4 * hh + e] = fmaf(dr[r], kv[hh][e], dq_acc[r][4 * hh + e]);
     }
+    __syncthreads();  // this stage and dS may be overwritten
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    const int il = 4 * ty + r;
+    const int il = ty + 16 * r;
     if (il >= qvalid) continue;
-    const size_t off = (static_cast<size_t>(bh) * p.Nq + i0 + il) * D + tx * CW;
+    const size_t off = (static_cast<size_t>(bh) * p.Nq + i0 + il) * D + 4 * tx;
 #pragma unroll
-    for (int c4 = 0; c4 < CW; c4 += 4)
-      *reinterpret_cast<float4*>(p.dq + off + c4) =
-          make_float4(dq_acc[r][c4] * p.scale, dq_acc[r][c4 + 1] * p.scale, dq_acc[r][c4 + 2] * p.scale,
-                      dq_acc[r][c4 + 3] * p.scale);
+    for (int hh = 0; hh < NH; ++hh)
+      *reinterpret_cast<float4*>(p.dq + off + 64 * hh) =
+          make_float4(dq_acc[r][4 * hh] * p.scale, dq_acc[r][4 * hh + 1] * p.scale, dq_acc[r][4 * hh + 2] * p.scale,
+                      dq_acc[r][4 * hh + 3] * p.scale);
   }
   // This grid may have started before the dK/dV grid finished; waiting for it here keeps every gradient
   // complete once this grid is, for the work that follows the backward on the stream.
