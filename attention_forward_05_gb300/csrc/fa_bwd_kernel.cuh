@@ -831,9 +831,11 @@ __global__ void __maxnreg__(C::MAXREG)
       commit(bar_drain);
       mbar_wait_drain(bar_drain, 0, p.err, WB_DRAIN);
     } else {
-      // dQ_t(j) once the warpgroup has written dS_t(j) (over dP_t), then, from the same lane and so behind
-      // it in the tensor pipe (MMAs issued by one thread run in issue order), dP_t(j+1) into the columns
-      // dQ_t(j) reads.
+      // dQ_t(j) once the warpgroup has written dS_t(j) (over dP_t), then, from the same lane, dP_t(j+1)
+      // into the columns dQ_t(j) reads as its A operand.  No barrier separates the two: this relies on the
+      // tensor core running the MMAs one thread issues in issue order (the PTX ISA states that order for
+      // MMAs into the same accumulator; these two write different ones), as the forward kernel's P V and
+      // next Q K^T over the aliased S / P columns do.
       bool ok = wait_all(bar_q, 0, WB_Q);
       if constexpr (C::ATMEM) {
 #pragma unroll
