@@ -1,6 +1,6 @@
 """The C ABI from C: include/fa.h compiles as strict C11 on its own, and a plain C program (no Python,
-no torch) builds against libfa and the CUDA runtime's C API; on a GPU it runs one fa_fwd and checks it
-against the oracle's C library."""
+no torch) builds against libfa and the CUDA runtime's C API; on a GPU it runs one fa_fwd and one
+fa_decode_splitkv (ragged chunks) and checks both against the oracle's C library."""
 import os
 import subprocess
 
